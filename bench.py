@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the paged quantized-KV hot path on one GB300 (or N, weak scaling).
+
+One step = one pass of the whole path over the long-context stress workload:
+kv_append_quant of an 8192-token chunk into a fragmented E4M3 pool, then
+paged_attention verify (q_len 5, causal among the draft) over 2 x 524288 +
+6 x 32768 cached tokens, 32 query / 8 KV heads, head_dim 128, 16-token pages,
+balanced split-KV merged by log-sum-exp.  Inputs are seeded synthetic data
+resident in HBM (2.55 GB of KV, larger than L2, so no L2 flush is needed).
+
+Prints one JSON line (rank 0).  Metric: effective KV GB/s of the step =
+algorithmic bytes (KV codes read by attention + the append's fp16 read and
+codes written + queries, outputs, block tables, slots) / device time per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pqkv|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged quantized-KV attention: effective KV GB/s (% of HBM peak), µs/step"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pqkv", "reference"], default="pqkv")
+    ap.add_argument("--workload", default="e4m3_verify_512k_stress")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed (one process per GPU; the path has no exchange step)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload set-up (seeded synthetic inputs, resident in HBM)
+# ---------------------------------------------------------------------------
+def setup(wname: str, device: str):
+    import numpy as np
+    import torch
+    import paged_quantized_kv_append_gb300 as pq
+    import workloads as W
+
+    w = W.workload(wname)
+    plan = W.plan_pool(w)
+    ks, vs = W.calibrated_scales(w, device)
+    pages = pq.new_pages(plan.num_pages, w.num_kv_heads, w.kv_dtype, device, fill=0)
+    for s, L in enumerate(w.seq_lens):
+        for a in range(0, L, 1 << 16):
+            b = min(L, a + (1 << 16))
+            k, v = W.kv_tokens(w, s, a, b, device)
+            slots = torch.from_numpy(W.slots_for(plan, s, a, b)).to(device)
+            pq.kv_append_quant(k, v, slots, w.kv_dtype, ks, vs, pages)
+    ctx = dict(w=w, plan=plan, ks=ks, vs=vs, pages=pages)
+    ctx["q"] = W.query(w, device)
+    ctx["out"] = torch.empty_like(ctx["q"])
+    ctx["bt"] = torch.from_numpy(plan.block_table).to(device)
+    ctx["seq_lens"] = torch.tensor(w.seq_lens, dtype=torch.int32, device=device)
+    if w.append_tokens:
+        ctx["ak"], ctx["av"] = W.append_chunk(w, device)
+        ctx["aslots"] = torch.from_numpy(plan.append_slots).to(device)
+    ctx["ws"] = pq.Workspace(device)
+    torch.cuda.synchronize()
+    return ctx
+
+
+def algorithmic_bytes(ctx):
+    w = ctx["w"]
+    B, H = w.num_seqs, w.num_kv_heads
+    attn = (w.kv_bytes() + 2 * ctx["q"].numel() * 2
+            + sum(w.pages_of(L) for L in w.seq_lens) * 4 + B * 4)
+    app = w.append_bytes(w.append_tokens) if w.append_tokens else 0
+    return attn, app
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("attention_impl.cuh", "pqkv_common.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_quantized_kv_append_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """DRAM bytes per attention launch from a committed ncu summary, if it was
+    taken on the current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
+    try:
+        d = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def hbm_peak():
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        return n
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def oracle_sample(wname: str, seconds: float, max_segments: int = 64):
+    """Time the oracle's paged attention over (sequence, kv-head) segments of
+    a 32768-token sequence of the workload until `seconds` have elapsed."""
+    import numpy as np
+    import oracle
+    import workloads as W
+
+    w = W.workload(wname)
+    plan = W.plan_pool(w)
+    s = int(np.argmin(w.seq_lens))
+    L = w.seq_lens[s]
+    n = w.pages_of(L)
+    rng = np.random.default_rng(0)
+    bt = rng.permutation(n).astype(np.int32)[None, :]
+    k, v = W.kv_tokens(w, s, 0, L, "cpu")
+    kscale = W.scale_from_amax(k.float().abs().max().item(), 448.0)
+    vscale = W.scale_from_amax(v.float().abs().max().item(), 448.0)
+    t = np.arange(L)
+    pool = oracle.new_pool(n, w.num_kv_heads, w.head_dim, w.kv_dtype)
+    pool = oracle.kv_append_quant(k.numpy(), v.numpy(), bt[0, t // 16].astype(np.int64) * 16 + t % 16,
+                                  w.kv_dtype, [kscale], [vscale], pool)
+    q = W.query(w, "cpu").numpy()[s * w.q_len:(s + 1) * w.q_len]
+    done, seg_bytes = 0, L * w.head_dim * 2 * w.elem_bytes
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds and done < max_segments:
+        h = done % w.num_kv_heads
+        oracle.paged_attention(q, pool, bt, [L], w.q_len, w.kv_dtype, [kscale], [vscale],
+                               heads=[h])
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": done * seg_bytes / dt / 1e9, "unit": UNIT, "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": "oracle paged_attention (float64 numpy) over %d (sequence, kv-head) segments "
+                      "of %d tokens (q_len %d, %d query rows each) of the workload; KV code "
+                      "bytes read / wall time" % (done, L, w.q_len, w.group * w.q_len),
+            "seconds": dt}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+    steps = []
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    last = None
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(args.workload, per_step, max_segments=8)
+        if i >= args.warmup:
+            steps.append(r)
+        last = r
+    value = statistics.median([r["value"] for r in steps])
+    sec = statistics.median([r["seconds"] for r in steps])
+    cb = dict(last)
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample": cb["sample"]},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_pqkv(args, rank, local, world):
+    import torch
+    import paged_quantized_kv_append_gb300 as pq
+    from paged_quantized_kv_append_gb300 import build as pqbuild
+
+    pqbuild.build()
+    pq.load_library()
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    ctx = setup(args.workload, dev)
+    w = ctx["w"]
+    stream = torch.cuda.current_stream()
+    attn_bytes, app_bytes = algorithmic_bytes(ctx)
+    launches_per_step = 1 + (1 if w.append_tokens else 0)
+
+    def step(ev=None):
+        if w.append_tokens:
+            pq.kv_append_quant(ctx["ak"], ctx["av"], ctx["aslots"], w.kv_dtype, ctx["ks"],
+                               ctx["vs"], ctx["pages"])
+        if ev is not None:
+            ev[0].record(stream)
+        pq.paged_attention(ctx["q"], ctx["pages"], ctx["bt"], ctx["seq_lens"], w.q_len,
+                           w.kv_dtype, ctx["ks"], ctx["vs"], ctx["out"],
+                           num_splits=args.num_splits, workspace=ctx["ws"],
+                           max_seq_len=max(w.seq_lens))
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(attn_ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_step = total_ms / args.steps
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_avg = statistics.mean(attn_ms)
+    step_bytes = attn_bytes + app_bytes
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {n: ctx[n].cpu().pin_memory() for n in ("q", "bt", "seq_lens")}
+        dev_in = {n: torch.empty_like(ctx[n]) for n in ("q", "bt", "seq_lens")}
+        if w.append_tokens:
+            for n in ("ak", "av", "aslots"):
+                host[n] = ctx[n].cpu().pin_memory()
+                dev_in[n] = torch.empty_like(ctx[n])
+        out_host = torch.empty(ctx["out"].shape, dtype=ctx["out"].dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for n, t in host.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            if w.append_tokens:
+                pq.kv_append_quant(dev_in["ak"], dev_in["av"], dev_in["aslots"], w.kv_dtype,
+                                   ctx["ks"], ctx["vs"], ctx["pages"])
+            pq.paged_attention(dev_in["q"], ctx["pages"], dev_in["bt"], dev_in["seq_lens"],
+                               w.q_len, w.kv_dtype, ctx["ks"], ctx["vs"], ctx["out"],
+                               num_splits=args.num_splits, workspace=ctx["ws"],
+                               max_seq_len=max(w.seq_lens))
+            out_host.copy_(ctx["out"], non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+            torch.cuda.synchronize()
+        el = max_over_ranks(time.perf_counter() - s0, world)
+        e2e = {"value": world * step_bytes * args.steps / el / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": el * 1e3 / args.steps}
+
+    if rank != 0:
+        return
+    peak, peak_src = hbm_peak()
+    achieved = attn_bytes / (attn_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+        "pct_of_hbm_peak": 100.0 * (step_bytes / (ms_step * 1e-3) / 1e9) / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 codes, f16 products, f32 accumulation" if w.kv_dtype == 1 else
+                 ("int8 codes, f16 products, f32 accumulation" if w.kv_dtype == 2 else "f16"),
+        "data": "synthetic",
+        "config": {"workload": w.name, "seq_lens": "2x524288+6x32768" if w.name.endswith("stress")
+                   else w.seq_lens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "page_size": w.page_size, "q_len": w.q_len,
+                   "append_tokens": w.append_tokens, "num_splits": args.num_splits,
+                   "attention_bytes": attn_bytes, "append_bytes": app_bytes,
+                   "l2": "inputs larger than L2 (%.2f GB of KV per step)" % (w.kv_bytes() / 1e9)},
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src
+                     if peak_src == "measured" else "fallback",
+                     "traffic": measured_traffic(), "attention_us": attn_avg * 1e3},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(args.workload, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_pqkv(args, rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -52,15 +52,19 @@ def kv_append_quant(k, v, slot_mapping, kv_dtype, k_scale, v_scale, pages):
     H = k.shape[1]
     ks = np.broadcast_to(np.asarray(k_scale, dtype=np.float32).reshape(-1), (H,))
     vs = np.broadcast_to(np.asarray(v_scale, dtype=np.float32).reshape(-1), (H,))
-    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
-        if slot < 0:
-            continue
-        page, off = divmod(int(slot), P)
-        if page >= out.shape[0]:
-            raise IndexError("slot %d outside the pool" % slot)
-        for h in range(H):
-            out[page, h, 0, off] = quantize(k[t, h], ks[h], kv_dtype)
-            out[page, h, 1, off] = quantize(v[t, h], vs[h], kv_dtype)
+    slots = np.asarray(slot_mapping, dtype=np.int64).reshape(-1)
+    keep = np.nonzero(slots >= 0)[0]
+    if keep.size == 0:
+        return out
+    if slots[keep].max() >= out.shape[0] * P:
+        raise IndexError("slot %d outside the pool" % slots[keep].max())
+    # a later token wins: keep only the last occurrence of each slot
+    _, last_rev = np.unique(slots[keep][::-1], return_index=True)
+    keep = np.sort(keep[::-1][last_rev])
+    page, off = np.divmod(slots[keep], P)
+    for h in range(H):
+        out[page, h, 0, off] = quantize(k[keep, h], ks[h], kv_dtype)
+        out[page, h, 1, off] = quantize(v[keep, h], vs[h], kv_dtype)
     return out
 
 

@@ -1,0 +1,301 @@
+// C-ABI entry points of libpqkv (declared in include/pqkv.h): argument
+// validation, TMA tensor-map encoding, grid sizing and workspace carve-up.
+// Everything the device computes happens in append.cu / attention_*.cu.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pqkv_internal.h"
+
+namespace pqkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxGrid = 4096;           // upper bound of the balanced grid
+constexpr int kMinPagesPerBlock = 16;    // smallest balanced share worth a block
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PQKV_ECUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev[dev].ready) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return PQKV_ECUDA;
+    g_dev[dev].sms = n;
+    g_dev[dev].ready = true;
+  }
+  *sms = g_dev[dev].sms;
+  return PQKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_bytes(int kv_dtype) { return kv_dtype == PQKV_KV_FP16 ? 2 : 1; }
+
+int blocks_per_sm(int kv_dtype, int nt, int num_seqs) {
+  switch (kv_dtype) {
+    case PQKV_KV_FP16: return attention_blocks_per_sm_fp16(nt, num_seqs);
+    case PQKV_KV_FP8_E4M3: return attention_blocks_per_sm_e4m3(nt, num_seqs);
+    case PQKV_KV_INT8: return attention_blocks_per_sm_int8(nt, num_seqs);
+  }
+  return 0;
+}
+
+// Sizes shared by the workspace query and the launch.
+struct AttnPlan {
+  int rows = 0, rp = 0, nt = 0;
+  int64_t slots = 0;        // partial-result slots
+  size_t counter_bytes = 0, o_bytes = 0, ml_bytes = 0, total = 0;
+};
+
+int plan_attention(int32_t num_seqs, int32_t q_len, int32_t hq, int32_t hkv, int32_t num_splits,
+                   int grid, AttnPlan* pl) {
+  pl->rows = (hq / hkv) * q_len;
+  pl->rp = rows_padded(pl->rows);
+  pl->nt = pl->rp / 8;
+  const int64_t segs = (int64_t)num_seqs * hkv;
+  if (num_splits == 1) {
+    pl->slots = 0;
+  } else if (num_splits > 1) {
+    pl->slots = segs * num_splits;             // slot = block index
+  } else {
+    pl->slots = segs + grid;                   // slot = segment + block index
+  }
+  if (pl->slots == 0) {
+    pl->total = 0;
+    return PQKV_OK;
+  }
+  pl->counter_bytes = PQKV_COUNTER_BYTES(num_seqs, hkv);
+  pl->o_bytes = (size_t)pl->slots * pl->rp * kHeadDim * 4;
+  pl->ml_bytes = (size_t)pl->slots * 2 * pl->rp * 4;
+  pl->total = pl->counter_bytes + ((pl->o_bytes + 255) & ~size_t(255)) + pl->ml_bytes;
+  return PQKV_OK;
+}
+
+int validate_common(int32_t head_dim, int32_t page_size, int32_t kv_dtype) {
+  if (kv_dtype < PQKV_KV_FP16 || kv_dtype > PQKV_KV_INT8) return PQKV_EINVAL;
+  if (head_dim != kHeadDim || page_size != kPageSize) return PQKV_EUNSUPPORTED;
+  return PQKV_OK;
+}
+
+int validate_heads(int32_t num_seqs, int32_t q_len, int32_t hq, int32_t hkv) {
+  if (num_seqs < 0 || q_len < 1 || hq < 1 || hkv < 1) return PQKV_EINVAL;
+  if (hq % hkv != 0) return PQKV_EINVAL;
+  if (num_seqs > PQKV_MAX_SEQS || q_len > PQKV_MAX_Q_LEN) return PQKV_ERANGE;
+  if ((hq / hkv) * q_len > PQKV_MAX_ROWS) return PQKV_EUNSUPPORTED;
+  return PQKV_OK;
+}
+
+}  // namespace
+}  // namespace pqkv
+
+using namespace pqkv;
+
+extern "C" int pqkv_kv_append_quant(const void* k, int64_t k_token_stride, const void* v,
+                                    int64_t v_token_stride, const int64_t* slot_mapping,
+                                    int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                                    int32_t scale_per_head, void* pages, int64_t num_pages,
+                                    int32_t page_size, int32_t* status, void* stream) {
+  int rc = validate_common(head_dim, page_size, kv_dtype);
+  if (rc) return rc;
+  if (num_tokens < 0 || num_kv_heads < 1 || num_pages < 0) return PQKV_EINVAL;
+  if (num_tokens == 0) return PQKV_OK;
+  if (!k || !v || !slot_mapping || !pages) return PQKV_EINVAL;
+  if (kv_dtype != PQKV_KV_FP16 && (!k_scale || !v_scale)) return PQKV_EINVAL;
+  if (k_token_stride < (int64_t)num_kv_heads * head_dim ||
+      v_token_stride < (int64_t)num_kv_heads * head_dim)
+    return PQKV_EINVAL;
+  if (k_token_stride % 8 || v_token_stride % 8) return PQKV_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(pages, 16) || !aligned(slot_mapping, 8))
+    return PQKV_EINVAL;
+  int sms = 0;
+  rc = current_device_sms(&sms);
+  if (rc) return rc;
+  AppendParams p;
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.k_stride = k_token_stride;
+  p.v_stride = v_token_stride;
+  p.slots = slot_mapping;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.scale_per_head = scale_per_head ? 1 : 0;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.pages = static_cast<uint8_t*>(pages);
+  p.num_pages = num_pages;
+  p.status = status;
+  const int64_t work = (int64_t)num_tokens * num_kv_heads * (kHeadDim / 16);
+  const int64_t blocks = (work + 255) / 256;
+  const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * 8);
+  if (launch_append(p, kv_dtype, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PQKV_ECUDA;
+  return PQKV_OK;
+}
+
+extern "C" size_t pqkv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len,
+                                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                                      int32_t head_dim, int32_t num_splits) {
+  if (head_dim != kHeadDim) return 0;
+  if (validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads)) return 0;
+  if (num_splits < 0 || num_splits > PQKV_MAX_SPLITS) return 0;
+  AttnPlan pl;
+  plan_attention(num_seqs, q_len, num_q_heads, num_kv_heads, num_splits, kMaxGrid, &pl);
+  return pl.total;
+}
+
+extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
+                                    int64_t num_pages, const int32_t* block_table,
+                                    int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                    int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                    int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                                    int32_t scale_per_head, int32_t num_splits,
+                                    int32_t max_seq_len, void* workspace, size_t workspace_bytes,
+                                    int32_t* status, void* stream) {
+  int rc = validate_common(head_dim, page_size, kv_dtype);
+  if (rc) return rc;
+  rc = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
+  if (rc) return rc;
+  if (num_splits < 0 || num_splits > PQKV_MAX_SPLITS) return PQKV_ERANGE;
+  if (num_seqs == 0) return PQKV_OK;
+  if (!q || !out || !pages || !block_table || !seq_lens) return PQKV_EINVAL;
+  if (kv_dtype != PQKV_KV_FP16 && (!k_scale || !v_scale)) return PQKV_EINVAL;
+  if (num_pages < 1 || num_pages > INT32_MAX || max_pages_per_seq < 1) return PQKV_EINVAL;
+  if ((int64_t)max_pages_per_seq * page_size > PQKV_MAX_SEQ_LEN + page_size) return PQKV_ERANGE;
+  if (max_seq_len < 0) return PQKV_EINVAL;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(pages, 16) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4))
+    return PQKV_EINVAL;
+
+  int sms = 0;
+  rc = current_device_sms(&sms);
+  if (rc) return rc;
+  AttnPlan pl;
+  const int rows = (num_q_heads / num_kv_heads) * q_len;
+  const int nt = rows_padded(rows) / 8;
+
+  // grid
+  int grid;
+  if (num_splits == 0) {
+    const int per_sm = blocks_per_sm(kv_dtype, nt, num_seqs);
+    if (per_sm <= 0) return PQKV_ECUDA;
+    const int64_t lmax = max_seq_len > 0 ? std::min<int64_t>(max_seq_len,
+                                                             (int64_t)max_pages_per_seq * page_size)
+                                         : (int64_t)max_pages_per_seq * page_size;
+    const int64_t units = (int64_t)num_seqs * num_kv_heads * ((lmax + page_size - 1) / page_size);
+    const int64_t want = (units + kMinPagesPerBlock - 1) / kMinPagesPerBlock;
+    const int64_t cap = std::min<int64_t>((int64_t)sms * per_sm, (int64_t)kMaxGrid);
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
+  } else {
+    const int64_t g = (int64_t)num_seqs * num_kv_heads * num_splits;
+    if (g > INT32_MAX) return PQKV_ERANGE;
+    grid = (int)g;
+  }
+  plan_attention(num_seqs, q_len, num_q_heads, num_kv_heads, num_splits, grid, &pl);
+  if (pl.total > 0) {
+    if (!workspace) return PQKV_EWORKSPACE;
+    if (!aligned(workspace, 256) || workspace_bytes < pl.total) return PQKV_EWORKSPACE;
+  }
+
+  // TMA map over the pool: [num_pages][Hkv][lines][128 bytes]
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return PQKV_ECUDA;
+  const int eb = elem_bytes(kv_dtype);
+  const cuuint32_t lines = (cuuint32_t)(2 * page_size * head_dim * eb / 128);
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  const cuuint64_t dims[4] = {(cuuint64_t)(128 / eb), lines, (cuuint64_t)num_kv_heads,
+                              (cuuint64_t)num_pages};
+  const cuuint64_t strides[3] = {128, (cuuint64_t)lines * 128,
+                                 (cuuint64_t)lines * 128 * num_kv_heads};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / eb), lines, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult cr = enc(&map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          4, const_cast<void*>(pages), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return PQKV_ECUDA;
+
+  AttnParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = static_cast<uint16_t*>(out);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = pl.total ? reinterpret_cast<int32_t*>(ws) : nullptr;
+  p.part_o = pl.total ? reinterpret_cast<float*>(ws + pl.counter_bytes) : nullptr;
+  p.part_ml = pl.total ? reinterpret_cast<float*>(ws + pl.counter_bytes +
+                                                  ((pl.o_bytes + 255) & ~size_t(255)))
+                       : nullptr;
+  p.status = status;
+  p.num_pages = num_pages;
+  p.bt_stride = max_pages_per_seq;
+  p.num_seqs = num_seqs;
+  p.q_len = q_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.rows = rows;
+  p.scale_per_head = scale_per_head ? 1 : 0;
+  p.num_splits = num_splits;
+  p.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+
+  cudaError_t e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (kv_dtype) {
+    case PQKV_KV_FP16: e = launch_attention_fp16(p, map, grid, nt, st); break;
+    case PQKV_KV_FP8_E4M3: e = launch_attention_e4m3(p, map, grid, nt, st); break;
+    default: e = launch_attention_int8(p, map, grid, nt, st); break;
+  }
+  return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
+}
+
+extern "C" const char* pqkv_status_string(int code) {
+  switch (code) {
+    case PQKV_OK: return "ok";
+    case PQKV_EINVAL: return "invalid argument (null/misaligned pointer or bad size)";
+    case PQKV_EUNSUPPORTED: return "unsupported configuration";
+    case PQKV_ERANGE: return "size outside the supported range";
+    case PQKV_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case PQKV_ECUDA: return "CUDA runtime call or kernel launch failed";
+    case PQKV_DEV_SLOT_RANGE: return "device: slot beyond the pool (token skipped)";
+    case PQKV_DEV_SEQ_RANGE: return "device: seq_len out of range (clamped)";
+    case PQKV_DEV_BAD_SCALE: return "device: scale not finite and positive";
+    case PQKV_DEV_TIMEOUT: return "device: pipeline wait timed out";
+    case PQKV_DEV_PAGE_RANGE: return "device: block-table page id out of range (read as zeros)";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* pqkv_version(void) { return "0.1.0"; }

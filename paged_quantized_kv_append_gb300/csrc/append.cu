@@ -1,0 +1,121 @@
+// kv_append_quant: quantize new K/V rows and scatter them into their pool
+// slots.  ReVolta README, "Weight and KV formats" ("E4M3 KV", "INT8 KV"): the
+// cache holds E4M3 codes under calibrated per-layer scales, INT8 codes under a
+// per-head scale, or plain fp16.
+//
+// One thread owns one 16-element vector of one (token, kv-head) row for both K
+// and V: it reads 32 B of fp16 per tensor (two 16-byte loads), forms the
+// correctly rounded fp32 quotient x / scale for each element, converts with
+// round-to-nearest-even and saturation, and stores 16 codes (one 16-byte
+// store; 32 B for fp16).  Consecutive threads cover consecutive vectors of a
+// row, so loads are fully coalesced and each (token, head) row lands as one
+// 128-byte line of its page tile.
+#include "pqkv_common.cuh"
+
+namespace pqkv {
+
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  // cvt packs its first source into the upper byte
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t int8_from_f32(float x) {
+  int i;
+  asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i) : "f"(x));  // NaN -> 0, saturating
+  i = max(-127, min(127, i));
+  return static_cast<uint32_t>(i) & 0xFFu;
+}
+
+__device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.4e38f; }
+
+// 16 fp16 values (as 8 words) -> 16 codes (4 words)
+template <int KVT>
+__device__ __forceinline__ uint4 quantize16(const uint4& a, const uint4& b, float scale) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[2 * i + j]);
+      f[2 * j] = __fdiv_rn(__low2float(h), scale);
+      f[2 * j + 1] = __fdiv_rn(__high2float(h), scale);
+    }
+    if (KVT == PQKV_KV_FP8_E4M3) {
+      out[i] = e4m3x2_from_f32(f[0], f[1]) | (e4m3x2_from_f32(f[2], f[3]) << 16);
+    } else {
+      out[i] = int8_from_f32(f[0]) | (int8_from_f32(f[1]) << 8) | (int8_from_f32(f[2]) << 16) |
+               (int8_from_f32(f[3]) << 24);
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <int KVT>
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  constexpr int kVecPerRow = kHeadDim / 16;
+  constexpr int kElem = (KVT == PQKV_KV_FP16) ? 2 : 1;
+  constexpr int64_t kTile = (int64_t)kPageSize * kHeadDim * kElem;  // one K (or V) tile
+  const int64_t total = (int64_t)p.num_tokens * p.num_kv_heads * kVecPerRow;
+  const int64_t pool_slots = p.num_pages * kPageSize;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % kVecPerRow);
+    const int64_t th = i / kVecPerRow;
+    const int h = (int)(th % p.num_kv_heads);
+    const int64_t t = th / p.num_kv_heads;
+    const int64_t slot = p.slots[t];
+    if (slot < 0) continue;
+    if (slot >= pool_slots) {
+      if (c == 0 && h == 0) report(p.status, PQKV_DEV_SLOT_RANGE);
+      continue;
+    }
+    const int64_t page = slot / kPageSize;
+    const int off = (int)(slot % kPageSize);
+    const uint4* ks = reinterpret_cast<const uint4*>(p.k + t * p.k_stride + h * kHeadDim + c * 16);
+    const uint4* vs = reinterpret_cast<const uint4*>(p.v + t * p.v_stride + h * kHeadDim + c * 16);
+    const uint4 k0 = __ldg(ks), k1 = __ldg(ks + 1);
+    const uint4 v0 = __ldg(vs), v1 = __ldg(vs + 1);
+    uint8_t* tile = p.pages + (page * p.num_kv_heads + h) * 2 * kTile;
+    uint8_t* kd = tile + (int64_t)off * kHeadDim * kElem + c * 16 * kElem;
+    uint8_t* vd = kd + kTile;
+    if (KVT == PQKV_KV_FP16) {
+      reinterpret_cast<uint4*>(kd)[0] = k0;
+      reinterpret_cast<uint4*>(kd)[1] = k1;
+      reinterpret_cast<uint4*>(vd)[0] = v0;
+      reinterpret_cast<uint4*>(vd)[1] = v1;
+    } else {
+      const int sh = p.scale_per_head ? h : 0;
+      const float kscale = __ldg(p.k_scale + sh);
+      const float vscale = __ldg(p.v_scale + sh);
+      if (!scale_ok(kscale) || !scale_ok(vscale)) {
+        if (c == 0) report(p.status, PQKV_DEV_BAD_SCALE);
+        continue;
+      }
+      *reinterpret_cast<uint4*>(kd) = quantize16<KVT>(k0, k1, kscale);
+      *reinterpret_cast<uint4*>(vd) = quantize16<KVT>(v0, v1, vscale);
+    }
+  }
+}
+
+cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream) {
+  switch (kv_dtype) {
+    case PQKV_KV_FP16:
+      append_kernel<PQKV_KV_FP16><<<grid, 256, 0, stream>>>(p);
+      break;
+    case PQKV_KV_FP8_E4M3:
+      append_kernel<PQKV_KV_FP8_E4M3><<<grid, 256, 0, stream>>>(p);
+      break;
+    case PQKV_KV_INT8:
+      append_kernel<PQKV_KV_INT8><<<grid, 256, 0, stream>>>(p);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pqkv

@@ -1,0 +1,16 @@
+// Paged attention instantiations for one KV format (kept in its own
+// translation unit so the formats compile in parallel).
+#include "attention_impl.cuh"
+
+namespace pqkv {
+
+cudaError_t launch_attention_e4m3(const AttnParams& p, const CUtensorMap& map, int grid, int nt,
+                                  cudaStream_t stream) {
+  return launch_attention_dtype<PQKV_KV_FP8_E4M3>(p, map, grid, nt, stream);
+}
+
+int attention_blocks_per_sm_e4m3(int nt, int num_seqs) {
+  return blocks_per_sm_dtype<PQKV_KV_FP8_E4M3>(nt, num_seqs);
+}
+
+}  // namespace pqkv

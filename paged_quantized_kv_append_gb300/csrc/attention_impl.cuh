@@ -1,0 +1,813 @@
+// Paged decode / speculative-verify attention over an FP16, E4M3 or INT8 KV
+// pool, with split-KV partitions merged by log-sum-exp.
+//
+// What it computes: ReVolta README, "Quick start" (MTP verify of 1 committed +
+// 4 draft positions with a causal mask among them, GQA) and "Weight and KV
+// formats" (KV stored compressed, widened to fp16 for the products); the split
+// of a sequence's keys with partial results combined afterwards is the
+// one-GPU counterpart of the decode-context-parallel split on the same page
+// ("Hardware", "Quick start").
+//
+// Design (GB300, sm_103a):
+//  * Work.  The key pages of every (sequence, kv-head) segment are laid end to
+//    end; in the balanced mode each of the C resident thread blocks takes one
+//    equal contiguous share of that list (so a block may finish one segment
+//    and start the next, and a long segment is shared by several blocks).  In
+//    the fixed mode block c takes partition c % k of segment c / k.  A block
+//    that holds a whole segment writes the output directly; otherwise it
+//    writes an unnormalised partial (O, m, l) and the last block to finish a
+//    segment (an atomic ticket; no block ever waits on another) merges the
+//    partials in a fixed order.
+//  * Data movement.  One producer warp streams the (page, kv-head) tiles --
+//    16 K rows followed by 16 V rows, 4 KB for 8-bit codes -- with 4-D TMA
+//    loads (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared
+//    memory stages guarded by mbarriers.  Block-table entries are read 32 at
+//    a time by the whole warp, one batch ahead.  Out-of-range page ids read
+//    as zeros (TMA bounds) and are reported.
+//  * Math.  Four consumer warps take pages round-robin.  Per page a warp
+//    dequantises the codes in registers (exact fp16), computes S^T = K Q^T
+//    with mma.sync m16n8k16 (tokens as M, the G*q_len query rows padded to 8,
+//    16 or 24 as N), keeps an fp32 online softmax in the log2 domain whose
+//    reference maximum is only raised when a score exceeds it by more than
+//    2^8 (so probabilities stay <= 256 in fp16), transposes P with movmatrix
+//    and accumulates O^T = V^T P^T with a second mma.  Warps merge their
+//    states through shared memory at the end of each segment share.
+#pragma once
+
+#include "pqkv_common.cuh"
+
+namespace pqkv {
+
+template <int KVT, int NT>
+struct AttnCfg {
+  static constexpr int kW = 4;                                     // consumer warps
+  static constexpr int kThreads = (kW + 1) * 32;
+  static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
+  static constexpr int kTileBytes = kLines * 128;
+  static constexpr int kStages = 8;
+  static constexpr int kRP = 8 * NT;                               // padded query rows
+  static constexpr bool kQRegs = false;     // Q fragments live in a shared table
+  static constexpr int kMinBlocks = NT == 1 ? 4 : 2;
+  // shared-memory carve-up (offsets from a 1024-aligned base)
+  static constexpr int kRingOff = 0;
+  static constexpr int kOOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kOBytes = kW * kRP * kHeadDim * 4;
+  static constexpr int kMLOff = kOOff + kOBytes;
+  static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
+  static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
+  static constexpr int kBarOff = kQfOff + (kQRegs ? 0 : 8 * NT * 32 * 8);
+  static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;
+  static constexpr int kMiscBytes = 64 + 2 * kStages * 4 + 2 * kRP * 4 + 128;
+  static constexpr int kPreOff = kMiscOff + kMiscBytes;
+  static __host__ __device__ constexpr int smem_bytes(int num_seqs) {
+    return kPreOff + (2 * num_seqs + 1) * 4 + 1024;
+  }
+};
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Work split: fragments of the concatenated (sequence, kv-head) page list
+// ---------------------------------------------------------------------------
+struct Frag {
+  int s, h, pg0, pg1;   // sequence, kv-head, page range [pg0, pg1)
+  int seg;              // s * H + h
+  int64_t a, b;         // the segment's span in the concatenated list
+};
+
+struct Split {
+  const int* pre;       // [B + 1] page prefix per sequence
+  int B, H;
+  int64_t P;            // total (page, kv-head) units
+  int C;                // blocks
+  int k;                // 0 = balanced
+
+  __device__ __forceinline__ int64_t start(int c) const { return (int64_t)c * P / C; }
+  // the block whose (non-empty) share holds unit x
+  __device__ __forceinline__ int cta_of(int64_t x) const { return (int)(((x + 1) * C - 1) / P); }
+  __device__ __forceinline__ int pages(int s) const { return pre[s + 1] - pre[s]; }
+
+  // number of partial results of segment seg
+  __device__ int count(int seg, int64_t a, int64_t b) const {
+    if (k > 0) return min(k, pages(seg / H));
+    int n = 0;
+    for (int64_t x = a; x < b; x = start(cta_of(x) + 1)) ++n;
+    return n;
+  }
+};
+
+struct FragIter {
+  Split sp;
+  int c;
+  int64_t x, e;
+  int s;
+  bool fixed_done;
+
+  __device__ void init(const Split& split, int cta) {
+    sp = split;
+    c = cta;
+    s = 0;
+    fixed_done = false;
+    if (sp.k == 0) {
+      x = sp.start(c);
+      e = sp.start(c + 1);
+    }
+  }
+
+  __device__ bool next(Frag& f) {
+    if (sp.k > 0) {
+      if (fixed_done) return false;
+      fixed_done = true;
+      const int seg = c / sp.k, p = c % sp.k;
+      if (seg >= sp.B * sp.H) return false;
+      f.s = seg / sp.H;
+      f.h = seg % sp.H;
+      const int np = sp.pages(f.s);
+      f.pg0 = (int)((int64_t)p * np / sp.k);
+      f.pg1 = (int)((int64_t)(p + 1) * np / sp.k);
+      f.seg = seg;
+      f.a = (int64_t)sp.pre[f.s] * sp.H + (int64_t)f.h * np;
+      f.b = f.a + np;
+      return f.pg1 > f.pg0;
+    }
+    if (x >= e) return false;
+    while ((int64_t)sp.pre[s + 1] * sp.H <= x) ++s;
+    const int np = sp.pages(s);
+    const int64_t base = (int64_t)sp.pre[s] * sp.H;
+    const int64_t off = x - base;
+    f.s = s;
+    f.h = (int)(off / np);
+    f.pg0 = (int)(off % np);
+    f.seg = s * sp.H + f.h;
+    f.a = base + (int64_t)f.h * np;
+    f.b = f.a + np;
+    const int64_t fe = min(e, f.b);
+    f.pg1 = f.pg0 + (int)(fe - x);
+    x = fe;
+    return true;
+  }
+};
+
+static_assert(sizeof(FragIter) + sizeof(Frag) <= 128, "iterator state must fit its smem slot");
+
+// ---------------------------------------------------------------------------
+// Per-page work of one consumer warp
+// ---------------------------------------------------------------------------
+// Physical head dims of the 4 K elements a lane feeds to k-step kk of QK^T
+// (order: b0.lo, b0.hi, b1.lo, b1.hi); they are 4 consecutive dims.
+template <int KVT>
+__device__ __forceinline__ int k_dim_base(int t, int kk) {
+  if (KVT == PQKV_KV_FP16) {
+    const int c1 = (t & 1) | ((t & 2) << 1);     // chunks {0,1,4,5} of a 64-dim line
+    const int q = kk >> 1;                        // which of the lane's 4 chunks
+    const int lh = q >> 1;                        // line half (dims 0-63 / 64-127)
+    const int ch = c1 + ((q & 1) << 1);
+    return 64 * lh + 8 * ch + 4 * (kk & 1);
+  } else {
+    return 32 * t + 4 * kk;
+  }
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* base, int line, int chunk) {
+  return *reinterpret_cast<const uint4*>(base + line * 128 + ((chunk ^ (line & 7)) << 4));
+}
+
+// Source of the Q^T B-fragments: registers (N <= 16) or a shared table.
+template <int NT, bool kRegs>
+struct QFrags {
+  uint32_t r[kRegs ? 8 : 1][NT][2];
+  const uint2* tab;   // [8][NT][32] when !kRegs
+  __device__ __forceinline__ void get(int kk, int nt, int lane, uint32_t& b0, uint32_t& b1) const {
+    if (kRegs) {
+      b0 = r[kRegs ? kk : 0][nt][0];
+      b1 = r[kRegs ? kk : 0][nt][1];
+    } else {
+      const uint2 q = tab[(kk * NT + nt) * 32 + lane];
+      b0 = q.x;
+      b1 = q.y;
+    }
+  }
+};
+
+template <int KVT>
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if (KVT == PQKV_KV_FP8_E4M3) e4m3_word(w, lo, hi);
+  else int8_word(w, lo, hi);
+}
+
+// S^T[16 tokens][8*NT rows] = K Q^T for one page tile.  Lane (g, t) feeds the
+// K rows of tokens g and g+8 and gets back S^T for tokens (g, g+8) and query
+// rows (8nt + 2t, 8nt + 2t + 1).  Codes are widened just before each k-step.
+template <int KVT, int NT, bool kRegs>
+__device__ __forceinline__ void page_qk(const uint8_t* T, int g, int t, int lane,
+                                        const QFrags<NT, kRegs>& qf, float (&sc)[NT][4]) {
+  if (KVT == PQKV_KV_FP16) {
+    const int c1 = (t & 1) | ((t & 2) << 1);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int lh = q >> 1, ch = c1 + ((q & 1) << 1);
+      const uint4 x = lds128(T, 2 * g + lh, ch);
+      const uint4 y = lds128(T, 2 * (g + 8) + lh, ch);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b0, b1;
+        qf.get(2 * q, nt, lane, b0, b1);
+        mma_16816(sc[nt], x.x, y.x, x.y, y.y, b0, b1);
+        qf.get(2 * q + 1, nt, lane, b0, b1);
+        mma_16816(sc[nt], x.z, y.z, x.w, y.w, b0, b1);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint4 x = lds128(T, g, 2 * t + half), y = lds128(T, g + 8, 2 * t + half);
+      const uint32_t wx[4] = {x.x, x.y, x.z, x.w}, wy[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        dequant_word<KVT>(wx[j], a0, a2);
+        dequant_word<KVT>(wy[j], a1, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t b0, b1;
+          qf.get(4 * half + j, nt, lane, b0, b1);
+          mma_16816(sc[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+    }
+  }
+}
+
+// Zero the halves of tokens at or beyond `valid` (tokens 2t, 2t+1 in a0/a1 and
+// 2t+8, 2t+9 in a2/a3 of a V^T fragment).
+struct VMask {
+  uint32_t m01, m89;
+  __device__ __forceinline__ void init(int t, int valid) {
+    m01 = (2 * t < valid ? 0x0000FFFFu : 0u) | (2 * t + 1 < valid ? 0xFFFF0000u : 0u);
+    m89 = (2 * t + 8 < valid ? 0x0000FFFFu : 0u) | (2 * t + 9 < valid ? 0xFFFF0000u : 0u);
+  }
+};
+
+// O^T[128 dims][8*NT rows] += V^T P^T for one page tile.  V^T m-tile mt holds
+// dims 16g + 2mt (A rows g) and 16g + 2mt + 1 (A rows g + 8) of tokens
+// (2t, 2t+1) and (2t+8, 2t+9).  When `masked`, tokens past the sequence end
+// are zeroed: their probability is 0, but a stale NaN code times 0 is NaN.
+template <int KVT, int NT>
+__device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
+                                        const uint32_t (&pb)[NT][2], bool masked, const VMask& vm,
+                                        float (&o)[8][NT][4]) {
+  auto mma_mt = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+    if (masked) {
+      a0 &= vm.m01;
+      a1 &= vm.m01;
+      a2 &= vm.m89;
+      a3 &= vm.m89;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+  };
+  if (KVT == PQKV_KV_FP16) {
+    const int lh = g >> 2, ch = 2 * (g & 3);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint4 A = lds128(T, 32 + 2 * (2 * t) + lh, ch + hh);
+      const uint4 B = lds128(T, 32 + 2 * (2 * t + 1) + lh, ch + hh);
+      const uint4 C = lds128(T, 32 + 2 * (2 * t + 8) + lh, ch + hh);
+      const uint4 D = lds128(T, 32 + 2 * (2 * t + 9) + lh, ch + hh);
+      const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w};
+      const uint32_t c[4] = {C.x, C.y, C.z, C.w}, d[4] = {D.x, D.y, D.z, D.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        mma_mt(4 * hh + j, __byte_perm(a[j], b[j], 0x5410), __byte_perm(a[j], b[j], 0x7632),
+               __byte_perm(c[j], d[j], 0x5410), __byte_perm(c[j], d[j], 0x7632));
+    }
+  } else {
+    const uint4 A = lds128(T, 16 + 2 * t, g), B = lds128(T, 17 + 2 * t, g);
+    const uint4 C = lds128(T, 24 + 2 * t, g), D = lds128(T, 25 + 2 * t, g);
+    const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w};
+    const uint32_t c[4] = {C.x, C.y, C.z, C.w}, d[4] = {D.x, D.y, D.z, D.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      if (KVT == PQKV_KV_FP8_E4M3) {
+        const uint32_t ab_lo = __byte_perm(a[wi], b[wi], 0x5140);
+        const uint32_t cd_lo = __byte_perm(c[wi], d[wi], 0x5140);
+        mma_mt(2 * wi, e4m3x2_to_f16x2(ab_lo), e4m3x2_to_f16x2(ab_lo >> 16),
+               e4m3x2_to_f16x2(cd_lo), e4m3x2_to_f16x2(cd_lo >> 16));
+        const uint32_t ab_hi = __byte_perm(a[wi], b[wi], 0x7362);
+        const uint32_t cd_hi = __byte_perm(c[wi], d[wi], 0x7362);
+        mma_mt(2 * wi + 1, e4m3x2_to_f16x2(ab_hi), e4m3x2_to_f16x2(ab_hi >> 16),
+               e4m3x2_to_f16x2(cd_hi), e4m3x2_to_f16x2(cd_hi >> 16));
+      } else {
+        mma_mt(2 * wi, i8pair(__byte_perm(a[wi], b[wi], 0x0400)),
+               i8pair(__byte_perm(a[wi], b[wi], 0x0501)), i8pair(__byte_perm(c[wi], d[wi], 0x0400)),
+               i8pair(__byte_perm(c[wi], d[wi], 0x0501)));
+        mma_mt(2 * wi + 1, i8pair(__byte_perm(a[wi], b[wi], 0x0602)),
+               i8pair(__byte_perm(a[wi], b[wi], 0x0703)), i8pair(__byte_perm(c[wi], d[wi], 0x0602)),
+               i8pair(__byte_perm(c[wi], d[wi], 0x0703)));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int KVT, int NT>
+__global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, AttnCfg<KVT, NT>::kMinBlocks)
+    paged_attention_kernel(const __grid_constant__ CUtensorMap map, const AttnParams p) {
+  using Cfg = AttnCfg<KVT, NT>;
+  constexpr int W = Cfg::kW, S = Cfg::kStages, RP = Cfg::kRP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem + Cfg::kRingOff;
+  float* sO = reinterpret_cast<float*>(smem + Cfg::kOOff);
+  float* sML = reinterpret_cast<float*>(smem + Cfg::kMLOff);
+  uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + Cfg::kQOff);
+  uint2* sQf = reinterpret_cast<uint2*>(smem + Cfg::kQfOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+  uint64_t* empty = full + S;
+  int* misc = reinterpret_cast<int*>(smem + Cfg::kMiscOff);
+  volatile int* abort_flag = misc + 0;
+  int* merge_flag = misc + 1;
+  uint32_t* issued = reinterpret_cast<uint32_t*>(misc + 16);
+  uint32_t* consumed = issued + S;
+  float* sMrow = reinterpret_cast<float*>(consumed + S);
+  float* sLrow = sMrow + RP;
+  int* pre = reinterpret_cast<int*>(smem + Cfg::kPreOff);
+  int* slen = pre + p.num_seqs + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = p.num_seqs, H = p.num_kv_heads;
+
+  // -- per-sequence lengths (clamped into the valid range) and page prefix
+  for (int s = tid; s < B; s += blockDim.x) {
+    int L = p.seq_lens[s];
+    const int Lmax = p.bt_stride * kPageSize;
+    if (L < p.q_len || L > Lmax) {
+      if (blockIdx.x == 0) report(p.status, PQKV_DEV_SEQ_RANGE);
+      L = max(p.q_len, min(L, Lmax));
+    }
+    slen[s] = L;
+    pre[s + 1] = (L + kPageSize - 1) / kPageSize;
+  }
+  if (tid == 0) {
+    pre[0] = 0;
+    misc[0] = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      issued[i] = 0;
+      consumed[i] = 0;
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < B; base += 32) {
+      int v = (base + lane < B) ? pre[base + lane + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (base + lane < B) pre[base + lane + 1] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+
+  Split sp;
+  sp.pre = pre;
+  sp.B = B;
+  sp.H = H;
+  sp.P = (int64_t)pre[B] * H;
+  sp.C = gridDim.x;
+  sp.k = p.num_splits;
+
+  if (warp == W) {
+    // ======================= producer warp =======================
+    if (lane == 0) prefetch_tensormap(&map);
+    const uint64_t policy = l2_evict_first_policy();
+    FragIter it;
+    it.init(sp, blockIdx.x);
+    Frag f;
+    uint32_t n = 0;
+    bool dead = false;
+    while (it.next(f)) {
+      const int* bt = p.block_table + (int64_t)f.s * p.bt_stride;
+      int nxt = (f.pg0 + lane < f.pg1) ? __ldg(bt + f.pg0 + lane) : 0;
+      for (int base = f.pg0; base < f.pg1; base += 32) {
+        const int id = nxt;
+        const int cnt = min(32, f.pg1 - base);
+        nxt = (base + 32 + lane < f.pg1) ? __ldg(bt + base + 32 + lane) : 0;
+        const bool bad = lane < cnt && (id < 0 || (int64_t)id >= p.num_pages);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, PQKV_DEV_PAGE_RANGE);
+        for (int j = 0; j < cnt; ++j, ++n) {
+          const int pid = __shfl_sync(0xffffffffu, id, j);
+          if (lane == 0 && !dead) {
+            const int stage = n % S;
+            const uint32_t round = n / S;
+            if (*abort_flag || !mbar_wait(&empty[stage], (round & 1) ^ 1)) {
+              dead = true;
+              *abort_flag = 1;
+              report(p.status, PQKV_DEV_TIMEOUT);
+            } else {
+              mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
+              tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, f.h, pid,
+                          policy);
+              issued[stage] += 1;
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ======================= consumer warps =======================
+    const int g = lane >> 2, t = lane & 3;
+    const int nthr = W * 32;
+    const int ctid = tid;  // 0 .. W*32-1
+    // The four consumer warps walk the fragments in lock step; one copy of the
+    // iterator lives in shared memory and consumer thread 0 advances it.
+    FragIter* sit = reinterpret_cast<FragIter*>(sLrow + RP);
+    Frag* sf = reinterpret_cast<Frag*>(sit + 1);
+    volatile int* has_frag = merge_flag + 1;
+    if (ctid == 0) sit->init(sp, blockIdx.x);
+    uint32_t n0 = 0;
+    int cur_seg = -1, cur_L = 0;
+    QFrags<NT, Cfg::kQRegs> qf;
+    qf.tab = sQf;
+    float qk_scale = 0.f, v_mult = 1.f;
+    int lim[NT][2];
+    int lim_min = 0;
+    bool dead = false;
+
+    for (;;) {
+      if (ctid == 0) *has_frag = sit->next(*sf) ? 1 : 0;
+      consumer_sync(nthr);
+      if (!*has_frag) break;
+      const int f_s = sf->s, f_h = sf->h, f_pg0 = sf->pg0, f_pg1 = sf->pg1, f_seg = sf->seg;
+      // ---- (re)load the query rows of this (sequence, kv-head)
+      if (f_seg != cur_seg) {
+        const int L = slen[f_s];
+        for (int v = ctid; v < RP * 16; v += nthr) {
+          const int r = v >> 4, c8 = v & 15;
+          uint4 val = make_uint4(0, 0, 0, 0);
+          if (r < p.rows) {
+            const int i = r / p.group, gh = r % p.group;
+            const int64_t row = ((int64_t)f_s * p.q_len + i) * p.num_q_heads + f_h * p.group + gh;
+            val = __ldg(reinterpret_cast<const uint4*>(p.q + row * kHeadDim) + c8);
+          }
+          reinterpret_cast<uint4*>(sQ)[v] = val;
+        }
+        consumer_sync(nthr);
+        if (warp == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int db = k_dim_base<KVT>(t, kk);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              sQf[(kk * NT + nt) * 32 + lane] =
+                  *reinterpret_cast<const uint2*>(sQ + (8 * nt + g) * kHeadDim + db);
+          }
+        }
+        const int sh = p.scale_per_head ? f_h : 0;
+        if (KVT == PQKV_KV_FP16) {
+          qk_scale = p.sm_scale_log2;
+          v_mult = 1.f;
+        } else {
+          const float ks = __ldg(p.k_scale + sh), vs = __ldg(p.v_scale + sh);
+          if (!(ks > 0.f && ks <= 3.4e38f && vs > 0.f && vs <= 3.4e38f))
+            report(p.status, PQKV_DEV_BAD_SCALE);
+          qk_scale = ks * p.sm_scale_log2;
+          v_mult = vs;
+        }
+        lim_min = L - p.q_len;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int r = 8 * nt + 2 * t + c;
+            lim[nt][c] = r < p.rows ? lim_min + r / p.group : 0x7fffffff;
+          }
+        cur_seg = f_seg;
+        cur_L = L;
+        consumer_sync(nthr);
+      }
+
+      // ---- stream this warp's pages of the fragment
+      float o[8][NT][4];
+      float mref[NT][2], lsum[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          mref[nt][c] = -INFINITY;
+          lsum[nt][c] = 0.f;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+      }
+      const int npg = f_pg1 - f_pg0;
+      const int first = (int)((warp - (int)(n0 % W) + W) % W);
+      for (int j = first; j < npg; j += W) {
+        const uint32_t gi = n0 + j;
+        const int stage = gi % S;
+        if (!dead) {
+          if (*abort_flag || !mbar_wait(&full[stage], (gi / S) & 1)) {
+            dead = true;
+            *abort_flag = 1;
+            report(p.status, PQKV_DEV_TIMEOUT);
+          }
+        }
+        if (dead) continue;
+        const uint8_t* T = ring + stage * Cfg::kTileBytes;
+        const int pos0 = (f_pg0 + j) * kPageSize;
+
+        // S^T = K Q^T
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+        page_qk<KVT, NT, Cfg::kQRegs>(T, g, t, lane, qf, sc);
+        // scale into log2 units and mask
+        const bool need_mask = pos0 + kPageSize - 1 > lim_min;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = sc[nt][e] * qk_scale;
+            if (need_mask) {
+              const int tok = pos0 + g + ((e & 2) ? 8 : 0);
+              if (tok > lim[nt][e & 1]) x = -INFINITY;
+            }
+            sc[nt][e] = x;
+          }
+        // page maximum per query row (uniform over the 8 lanes holding the row)
+        float pm[NT][2];
+        bool raise = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float m = fmaxf(sc[nt][c], sc[nt][c + 2]);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            pm[nt][c] = m;
+            raise |= m > mref[nt][c] + 8.f;
+          }
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              if (pm[nt][c] > mref[nt][c] + 8.f) {
+                const float fct = ex2(mref[nt][c] - pm[nt][c]);
+                mref[nt][c] = pm[nt][c];
+                lsum[nt][c] *= fct;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                  o[mt][nt][c] *= fct;
+                  o[mt][nt][c + 2] *= fct;
+                }
+              }
+            }
+        }
+        // probabilities (<= 2^8), row sums, and P^T -> B fragments
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float pr[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float mr = mref[nt][e & 1];
+            pr[e] = ex2(sc[nt][e] - (mr == -INFINITY ? 0.f : mr));
+          }
+          lsum[nt][0] += pr[0] + pr[2];
+          lsum[nt][1] += pr[1] + pr[3];
+          pb[nt][0] = movmatrix_trans(pack_half2(pr[0], pr[1]));
+          pb[nt][1] = movmatrix_trans(pack_half2(pr[2], pr[3]));
+        }
+        // O^T += V^T P^T
+        {
+          const bool tail = pos0 + kPageSize > cur_L;
+          VMask vm;
+          vm.init(t, cur_L - pos0);
+          page_pv<KVT, NT>(T, g, t, pb, tail, vm, o);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          consumed[stage] += 1;
+          mbar_arrive(&empty[stage]);
+        }
+      }
+      n0 += npg;
+
+      // ---- combine the warps' states of this fragment
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float l = lsum[nt][c];
+          l += __shfl_xor_sync(0xffffffffu, l, 4);
+          l += __shfl_xor_sync(0xffffffffu, l, 8);
+          l += __shfl_xor_sync(0xffffffffu, l, 16);
+          const int r = 8 * nt + 2 * t + c;
+          if (g == 0) {
+            sML[(warp * 2 + 0) * RP + r] = mref[nt][c];
+            sML[(warp * 2 + 1) * RP + r] = l;
+          }
+          float* dst = sO + ((size_t)warp * RP + r) * kHeadDim + 16 * g;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            *reinterpret_cast<float4*>(dst + 4 * k4) =
+                make_float4(o[2 * k4][nt][c], o[2 * k4][nt][c + 2], o[2 * k4 + 1][nt][c],
+                            o[2 * k4 + 1][nt][c + 2]);
+        }
+      consumer_sync(nthr);
+
+      const int cnt = sp.count(f_seg, sf->a, sf->b);
+      const int slot = sp.k > 0 ? (int)blockIdx.x : f_seg + (int)blockIdx.x;
+      const int64_t out_row0 = (int64_t)f_s * p.q_len;
+      {
+        const int d = ctid;  // one head dim per consumer thread
+        for (int r = 0; r < p.rows; ++r) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
+          float acc = 0.f, l = 0.f;
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            const float mw = sML[(w * 2) * RP + r];
+            const float sc = mw == -INFINITY ? 0.f : ex2(mw - M);
+            acc += sc * sO[((size_t)w * RP + r) * kHeadDim + d];
+            l += sc * sML[(w * 2 + 1) * RP + r];
+          }
+          if (cnt == 1) {
+            const int i = r / p.group, gh = r % p.group;
+            const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+            const float val = l > 0.f ? acc / l * v_mult : 0.f;
+            p.out[orow * kHeadDim + d] = __half_as_ushort(__float2half_rn(val));
+          } else {
+            p.part_o[((size_t)slot * RP + r) * kHeadDim + d] = acc;
+            if (d == 0) {
+              p.part_ml[(size_t)slot * 2 * RP + r] = M;
+              p.part_ml[(size_t)slot * 2 * RP + RP + r] = l;
+            }
+          }
+        }
+      }
+      if (cnt > 1) {
+        __threadfence();
+        consumer_sync(nthr);
+        if (ctid == 0) {
+          const int ticket = atomicAdd(p.counters + f_seg, 1);
+          *merge_flag = (ticket == cnt - 1);
+        }
+        consumer_sync(nthr);
+        if (*merge_flag) {
+          __threadfence();
+          // gather the segment's partial slots (fixed order) into shared memory
+          int* slots = reinterpret_cast<int*>(sO);
+          if (ctid == 0) {
+            int nsl = 0;
+            if (sp.k > 0) {
+              const int np = sp.pages(f_s);
+              for (int q = 0; q < sp.k; ++q)
+                if ((int64_t)(q + 1) * np / sp.k > (int64_t)q * np / sp.k)
+                  slots[nsl++] = f_seg * sp.k + q;
+            } else {
+              for (int64_t x = sf->a; x < sf->b;) {
+                const int cc = sp.cta_of(x);
+                slots[nsl++] = f_seg + cc;
+                x = sp.start(cc + 1);
+              }
+            }
+          }
+          consumer_sync(nthr);
+          // per-row maximum and normaliser
+          if (ctid < p.rows) {
+            const int r = ctid;
+            float M = -INFINITY;
+            for (int q = 0; q < cnt; ++q)
+              M = fmaxf(M, __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + r));
+            float l = 0.f;
+            for (int q = 0; q < cnt; ++q) {
+              const float mq = __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + r);
+              if (mq != -INFINITY)
+                l += ex2(mq - M) * __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + RP + r);
+            }
+            sMrow[r] = M;
+            sLrow[r] = l;
+          }
+          consumer_sync(nthr);
+          const int dq = ctid & 31, rg = ctid >> 5;
+          for (int r = rg; r < p.rows; r += W) {
+            const float M = sMrow[r];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int q = 0; q < cnt; ++q) {
+              const size_t sl = slots[q];
+              const float mq = __ldcg(p.part_ml + sl * 2 * RP + r);
+              const float wq = mq == -INFINITY ? 0.f : ex2(mq - M);
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                          p.part_o + (sl * RP + r) * kHeadDim) +
+                                      dq);
+              acc.x += wq * v.x;
+              acc.y += wq * v.y;
+              acc.z += wq * v.z;
+              acc.w += wq * v.w;
+            }
+            const float inv = sLrow[r] > 0.f ? v_mult / sLrow[r] : 0.f;
+            const int i = r / p.group, gh = r % p.group;
+            const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+            __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
+            __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+          }
+          if (ctid == 0) p.counters[f_seg] = 0;
+        }
+      }
+      consumer_sync(nthr);
+    }
+  }
+
+  // ---- drain: never leave with a tile copy in flight
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    for (int i = 0; i < S; ++i)
+      if (issued[i] > consumed[i]) (void)mbar_wait(&full[i], (issued[i] - 1) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int KVT, int NT>
+cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& map, int grid,
+                               cudaStream_t stream) {
+  using Cfg = AttnCfg<KVT, NT>;
+  static bool attr_set = false;
+  const int smem = Cfg::smem_bytes(p.num_seqs);
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<KVT, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::smem_bytes(PQKV_MAX_SEQS));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  paged_attention_kernel<KVT, NT><<<grid, Cfg::kThreads, smem, stream>>>(map, p);
+  return cudaGetLastError();
+}
+
+template <int KVT, int NT>
+int blocks_per_sm_t(int num_seqs) {
+  using Cfg = AttnCfg<KVT, NT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(paged_attention_kernel<KVT, NT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::smem_bytes(PQKV_MAX_SEQS)) != cudaSuccess)
+      return 0;
+    attr_set = true;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<KVT, NT>,
+                                                    Cfg::kThreads,
+                                                    Cfg::smem_bytes(num_seqs)) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int KVT>
+cudaError_t launch_attention_dtype(const AttnParams& p, const CUtensorMap& map, int grid, int nt,
+                                   cudaStream_t stream) {
+  switch (nt) {
+    case 1: return launch_attention_t<KVT, 1>(p, map, grid, stream);
+    case 2: return launch_attention_t<KVT, 2>(p, map, grid, stream);
+    case 3: return launch_attention_t<KVT, 3>(p, map, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int KVT>
+int blocks_per_sm_dtype(int nt, int num_seqs) {
+  switch (nt) {
+    case 1: return blocks_per_sm_t<KVT, 1>(num_seqs);
+    case 2: return blocks_per_sm_t<KVT, 2>(num_seqs);
+    case 3: return blocks_per_sm_t<KVT, 3>(num_seqs);
+    default: return 0;
+  }
+}
+
+}  // namespace pqkv

@@ -1,0 +1,169 @@
+// Device helpers shared by the append and attention kernels: inline PTX for
+// mbarriers, TMA tile loads, warp-level mma / movmatrix, and the 8-bit KV code
+// conversions.  sm_103a only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pqkv_internal.h"
+
+namespace pqkv {
+
+// ---------------------------------------------------------------------------
+// status word
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void report(int32_t* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses and mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until the phase of the given parity has completed.  Gives up after
+// kWaitLimitNs of wall time and returns false; the caller reports
+// PQKV_DEV_TIMEOUT and stops.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA: 4-D tiled load of one (page, kv-head) K+V tile into shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// warp-level tensor-core products
+// ---------------------------------------------------------------------------
+// D = A(16x16, row) * B(16x8, col) + D ; fp16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row-pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// 8-bit code -> fp16 conversions (exact: every E4M3 value and every integer
+// in [-127, 127] is an fp16 value)
+// ---------------------------------------------------------------------------
+// two E4M3 codes (low byte -> low half) to an f16x2
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes_low16) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(r)
+      : "r"(two_codes_low16));
+  return r;
+}
+
+// E4M3: 4 codes of a word -> (d0,d1), (d2,d3)
+__device__ __forceinline__ void e4m3_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_to_f16x2(w);
+  hi = e4m3x2_to_f16x2(w >> 16);
+}
+
+// INT8: code c becomes the fp16 1024 + (c + 128) by placing (c ^ 0x80) under
+// the fp16 exponent byte 0x64; 1152 is then subtracted exactly.
+// t = [c0, ?, c1, ?] (raw codes in bytes 0 and 2) -> f16x2 (c0, c1)
+__device__ __forceinline__ uint32_t i8pair(uint32_t t) {
+  uint32_t u = (t & 0x00FF00FFu) ^ 0x64806480u;
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  h = __hsub2(h, __half2(__half(1152.0f), __half(1152.0f)));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// INT8: 4 codes of a word -> (d0,d1), (d2,d3)
+__device__ __forceinline__ void int8_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = i8pair(__byte_perm(w, 0, 0x0100));
+  hi = i8pair(__byte_perm(w, 0, 0x0302));
+}
+
+}  // namespace pqkv

@@ -1,0 +1,74 @@
+// Internal declarations shared by the C-ABI layer and the kernel translation
+// units.  Not part of the public interface (include/pqkv.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pqkv.h"
+
+namespace pqkv {
+
+constexpr int kHeadDim = 128;
+constexpr int kPageSize = 16;
+
+struct AppendParams {
+  const uint16_t* k;        // fp16 bits
+  const uint16_t* v;
+  int64_t k_stride;         // elements between tokens
+  int64_t v_stride;
+  const int64_t* slots;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t scale_per_head;
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  uint8_t* pages;
+  int64_t num_pages;
+  int32_t* status;
+};
+
+struct AttnParams {
+  const uint16_t* q;        // fp16 bits [B*q_len][Hq][128]
+  uint16_t* out;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t* counters;        // [B*Hkv] merge tickets (workspace)
+  float* part_o;            // [slots][RP][128] unnormalised partial outputs
+  float* part_ml;           // [slots][2][RP]   running max (log2 units) and sum
+  int32_t* status;
+  int64_t num_pages;
+  int32_t bt_stride;        // max_pages_per_seq
+  int32_t num_seqs;
+  int32_t q_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;            // num_q_heads / num_kv_heads
+  int32_t rows;             // group * q_len
+  int32_t scale_per_head;
+  int32_t num_splits;       // 0: balanced shares, k >= 1: k partitions per (seq, head)
+  float sm_scale_log2;      // log2(e) / sqrt(head_dim)
+};
+
+// Host launchers (one per KV format), defined in the attention translation units.
+cudaError_t launch_attention_fp16(const AttnParams& p, const CUtensorMap& map, int grid,
+                                  int nt, cudaStream_t stream);
+cudaError_t launch_attention_e4m3(const AttnParams& p, const CUtensorMap& map, int grid,
+                                  int nt, cudaStream_t stream);
+cudaError_t launch_attention_int8(const AttnParams& p, const CUtensorMap& map, int grid,
+                                  int nt, cudaStream_t stream);
+// Resident blocks per SM of the attention kernel for a KV format, n-tile
+// count and number of sequences (0 if the query fails).
+int attention_blocks_per_sm_fp16(int nt, int num_seqs);
+int attention_blocks_per_sm_e4m3(int nt, int num_seqs);
+int attention_blocks_per_sm_int8(int nt, int num_seqs);
+
+cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream);
+
+inline int rows_padded(int rows) { return ((rows + 7) / 8) * 8; }
+
+}  // namespace pqkv

@@ -1,0 +1,173 @@
+"""paged_attention on the GPU against the float64 oracle.
+
+Bar: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise, plus a relative L2
+bound of 1e-2 (the absolute term alone would let near-uniform long-context
+outputs pass trivially), and a "needle" variant that makes outputs O(1).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.helpers import Case, assert_close, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {  # context scale per workload: small enough for the oracle, several tiles + ragged tail
+    "tiny_fp16_decode": 1.0,
+    "e4m3_decode_b8": 0.05,
+    "e4m3_verify_131k": 0.01,
+    "int8_decode_append_262k": 0.004,
+    "e4m3_verify_512k_stress": 0.004,
+}
+
+_cases = {}
+
+
+def case(name):
+    if name not in _cases:
+        _cases[name] = Case(W.workload(name, scale=SMALL[name]))
+    return _cases[name]
+
+
+@pytest.mark.parametrize("name", W.WORKLOAD_NAMES)
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_small_workloads_match_oracle(name, num_splits):
+    c = case(name)
+    assert np.array_equal(c.gpu_pool_bytes(), c.pool_o)
+    ref = c.oracle_attention()
+    out = c.attention(num_splits=num_splits)
+    assert_close(out, ref, "%s splits=%d" % (name, num_splits))
+
+
+@pytest.mark.parametrize("splits", [2, 7, 64])
+def test_split_count_invariance(splits):
+    c = case("e4m3_verify_512k_stress")
+    a = c.attention(num_splits=1).float()
+    b = c.attention(num_splits=splits).float()
+    assert_close(b, a.cpu().numpy().astype(np.float64), "splits %d vs 1" % splits)
+
+
+def test_bitwise_deterministic_and_page_order_invariant():
+    c = case("e4m3_verify_131k")
+    a = c.attention(num_splits=0)
+    b = c.attention(num_splits=0)
+    assert torch.equal(a, b)
+    # move every page to a new place in the pool: the output must not change
+    pq = require_gpu()
+    perm = np.random.default_rng(9).permutation(c.plan.num_pages)      # new -> old
+    inv = np.argsort(perm)
+    pages2 = c.pages[torch.from_numpy(perm).cuda()].contiguous()
+    bt2 = np.where(c.plan.block_table >= 0, inv[np.maximum(c.plan.block_table, 0)], -1)
+    out = torch.empty_like(c.q)
+    pq.paged_attention(c.q, pages2, torch.from_numpy(bt2.astype(np.int32)).cuda(), c.seq_lens,
+                       c.w.q_len, c.w.kv_dtype, c.ks, c.vs, out, num_splits=0)
+    assert torch.equal(out, a)
+
+
+@pytest.mark.parametrize("kv_dtype", [W.FP16, W.FP8_E4M3, W.INT8])
+@pytest.mark.parametrize("q_len,G", [(1, 1), (1, 4), (5, 4), (1, 8), (3, 8), (8, 2), (2, 12)])
+def test_row_shapes(kv_dtype, q_len, G):
+    # every padded-row width (8, 16, 24) and ragged lengths, incl. L == q_len
+    w = W.Workload("shape", 40 + q_len * 10 + G, [q_len, 17, 100, 333], 2 * G, 2, q_len, kv_dtype,
+                   outliers=kv_dtype != W.FP16, pool_slack=0.3)
+    c = Case(w)
+    for ns in (0, 1, 2):
+        assert_close(c.attention(num_splits=ns), c.oracle_attention(), "q_len %d G %d" % (q_len, G))
+
+
+def test_needle_outputs_are_order_one():
+    # every query row of a sequence is the same vector u; 8 keys per sequence
+    # (two inside the draft window) are 3u for every kv-head, so they take most
+    # of the softmax mass and the outputs are O(1) instead of ~1/sqrt(L).  The
+    # edits are made from CPU data and applied to both pools.
+    pq = require_gpu()
+    w = W.workload("e4m3_verify_512k_stress", scale=0.004)
+    c = Case(w)
+    rng = np.random.default_rng(4)
+    ks, vs = c.ks.cpu().numpy(), c.vs.cpu().numpy()
+    q = c.q.cpu().clone()
+    for s, L in enumerate(w.seq_lens):
+        u = torch.from_numpy(rng.normal(0, 1, 128).astype(np.float16))
+        q[s * w.q_len:(s + 1) * w.q_len] = u
+        pos = np.concatenate([rng.choice(L - w.q_len, 6, replace=False), [L - 3, L - 1]])
+        k0, v0 = W.kv_tokens(w, s, 0, L, "cpu")
+        fk = k0[pos].clone()
+        fk[:] = (u.float() * 3.0).half()
+        fv = v0[pos].contiguous()
+        slots = W.slots_for(c.plan, s, 0, L)[pos]
+        c.pool_o = oracle.kv_append_quant(fk.numpy(), fv.numpy(), slots, w.kv_dtype, ks, vs, c.pool_o)
+        pq.kv_append_quant(fk.cuda(), fv.cuda(), torch.from_numpy(slots).cuda(), w.kv_dtype,
+                           c.ks, c.vs, c.pages)
+    c.q = q.cuda()
+    assert np.array_equal(c.gpu_pool_bytes(), c.pool_o)
+    ref = c.oracle_attention()
+    assert np.abs(ref).max() > 0.3
+    for ns in (0, 1, 5):
+        assert_close(c.attention(num_splits=ns), ref, "needle splits %d" % ns)
+
+
+def test_every_e4m3_code_in_k_and_v():
+    # K and V tiles filled with all 256 codes (NaN codes excluded): checks the
+    # in-register widening of every code, subnormals and -0 included
+    pq = require_gpu()
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    L = 64
+    num_pages = 4
+    rng = np.random.default_rng(6)
+    pool = np.zeros((num_pages, 1, 2, 16, 128), np.uint8)
+    tok = rng.choice(codes, size=(L, 2, 128))
+    for j in range(L):
+        pool[j // 16, 0, 0, j % 16] = tok[j, 0]
+        pool[j // 16, 0, 1, j % 16] = tok[j, 1]
+    q = torch.from_numpy(rng.normal(0, 0.02, (1, 4, 128)).astype(np.float16)).cuda()
+    bt = torch.tensor([[0, 1, 2, 3]], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+    ks = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    vs = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    out = torch.empty_like(q)
+    pq.paged_attention(q, torch.from_numpy(pool).cuda(), bt, sl, 1, W.FP8_E4M3, ks, vs, out)
+    ref = oracle.paged_attention(q.cpu().numpy(), pool, bt.cpu().numpy(), [L], 1, W.FP8_E4M3,
+                                 [0.01], [0.5])
+    assert_close(out, ref, "all codes")
+
+
+def test_stale_nan_codes_past_the_end_are_ignored():
+    pq = require_gpu()
+    w = W.Workload("nan_tail", 77, [37, 50], 8, 2, 5, W.FP8_E4M3, pool_slack=0.5)
+    c = Case(w, with_oracle=True, fill=0x7F)     # every unwritten code is NaN
+    assert_close(c.attention(num_splits=0), c.oracle_attention(), "NaN tail")
+
+
+def test_out_of_range_page_id_reads_zeros_and_reports():
+    pq = require_gpu()
+    w = W.Workload("badpage", 78, [40], 4, 1, 1, W.INT8, pool_slack=0.5)
+    c = Case(w)
+    bt = c.bt.clone()
+    bt[0, 1] = 10 ** 6
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(c.q)
+    pq.paged_attention(c.q, c.pages, bt, c.seq_lens, 1, W.INT8, c.ks, c.vs, out, status=status)
+    assert "block-table page id out of range" in pq.status_bits(status)
+    pool = c.pool_o.copy()
+    bt_np = c.plan.block_table.copy()
+    spare = pool.shape[0]
+    pool = np.concatenate([pool, np.zeros_like(pool[:1])])
+    bt_np[0, 1] = spare
+    ref = oracle.paged_attention(c.q.cpu().numpy(), pool, bt_np, w.seq_lens, 1, W.INT8,
+                                 c.ks.cpu().numpy(), c.vs.cpu().numpy())
+    assert_close(out, ref, "zero page")
+
+
+def test_host_validation_errors():
+    pq = require_gpu()
+    c = case("tiny_fp16_decode")
+    out = torch.empty_like(c.q)
+    with pytest.raises(ValueError):
+        pq.paged_attention(c.q, c.pages, c.bt, c.seq_lens, 2, W.FP16, c.ks, c.vs, out)
+    with pytest.raises(ValueError):
+        pq.paged_attention(c.q[:, :7], c.pages, c.bt, c.seq_lens, 1, W.FP16, c.ks, c.vs, out)
+    q9 = torch.zeros((1, 9 * 8, 128), dtype=torch.float16, device="cuda")   # 72 rows per kv-head
+    with pytest.raises(ValueError):
+        pq.paged_attention(q9, c.pages, c.bt, c.seq_lens, 1, W.FP16, c.ks, c.vs, torch.empty_like(q9))
