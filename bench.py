@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["pqkv", "reference"], default="pqkv")
     ap.add_argument("--workload", default="e4m3_verify_512k_stress")
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="context-length scale of the workload (1.0 = the full workload; "
+                         "smaller values are for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -135,13 +138,13 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload set-up (seeded synthetic inputs, resident in HBM)
 # ---------------------------------------------------------------------------
-def setup(wname: str, device: str):
+def setup(wname: str, device: str, scale: float = 1.0):
     import numpy as np
     import torch
     import paged_quantized_kv_append_gb300 as pq
     import workloads as W
 
-    w = W.workload(wname)
+    w = W.workload(wname, scale)
     plan = W.plan_pool(w)
     ks, vs = W.calibrated_scales(w, device)
     pages = pq.new_pages(plan.num_pages, w.num_kv_heads, w.kv_dtype, device, fill=0)
@@ -289,7 +292,7 @@ def run_pqkv(args, rank, local, world):
     pq.load_library()
     torch.cuda.set_device(local)
     dev = "cuda:%d" % local
-    ctx = setup(args.workload, dev)
+    ctx = setup(args.workload, dev, args.scale)
     w = ctx["w"]
     stream = torch.cuda.current_stream()
     attn_bytes, app_bytes = algorithmic_bytes(ctx)
@@ -385,7 +388,8 @@ def run_pqkv(args, rank, local, world):
         "dtype": "e4m3 codes, f16 products, f32 accumulation" if w.kv_dtype == 1 else
                  ("int8 codes, f16 products, f32 accumulation" if w.kv_dtype == 2 else "f16"),
         "data": "synthetic",
-        "config": {"workload": w.name, "seq_lens": "2x524288+6x32768" if w.name.endswith("stress")
+        "config": {"workload": w.name, "scale": args.scale,
+                   "seq_lens": "2x524288+6x32768" if (w.name.endswith("stress") and args.scale == 1.0)
                    else w.seq_lens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "page_size": w.page_size, "q_len": w.q_len,
                    "append_tokens": w.append_tokens, "num_splits": args.num_splits,

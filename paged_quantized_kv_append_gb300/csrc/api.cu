@@ -15,7 +15,7 @@ namespace pqkv {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxGrid = 4096;           // upper bound of the balanced grid
+constexpr int kMaxGrid = 1024;           // upper bound of the balanced grid
 constexpr int kMinPagesPerBlock = 16;    // smallest balanced share worth a block
 
 struct DeviceInfo {

@@ -40,32 +40,47 @@ namespace pqkv {
 
 template <int KVT, int NT>
 struct AttnCfg {
-  static constexpr int kW = 4;                                     // consumer warps
-  static constexpr int kThreads = (kW + 1) * 32;
+  // One block per SM.  Every warp is a consumer and feeds its own slice of the
+  // TMA ring: page i of the block goes to warp i % kW and stage i % kStages,
+  // and kStages is a multiple of kW, so each stage always belongs to one warp
+  // (an mbarrier phase is tracked by one parity bit; a stage shared by warps
+  // could be waited on for a later round while an earlier load is still in
+  // flight).  Warp counts follow the register need of the row width and are
+  // multiples of 4, because registers are allotted per scheduler (a quarter
+  // of the SM): 8 warps get 255 registers each, 12 get 168, 16 get 128.
+  static constexpr int kW = (KVT == PQKV_KV_FP16) ? 8 : (NT == 1 ? 16 : (NT == 2 ? 12 : 8));
+  static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
   static constexpr int kTileBytes = kLines * 128;
-  static constexpr int kStages = 8;
+  static constexpr int kStagesPerWarp = (KVT == PQKV_KV_FP16) ? 2 : (kW <= 8 ? 4 : 3);
+  static constexpr int kStages = kW * kStagesPerWarp;
   static constexpr int kRP = 8 * NT;                               // padded query rows
   static constexpr bool kQRegs = false;     // Q fragments live in a shared table
-  static constexpr int kMinBlocks = NT == 1 ? 4 : 2;
+  static constexpr int kQfBytes = 8 * NT * 32 * 8;
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kRingOff = 0;
   static constexpr int kOOff = kRingOff + kStages * kTileBytes;
-  static constexpr int kOBytes = kW * kRP * kHeadDim * 4;
+  static constexpr int kOBytes = kRP * kHeadDim * 4;     // one warp's O, summed in turn
   static constexpr int kMLOff = kOOff + kOBytes;
   static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
   static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
-  static constexpr int kBarOff = kQfOff + (kQRegs ? 0 : 8 * NT * 32 * 8);
-  static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kMiscBytes = 64 + 2 * kStages * 4 + 2 * kRP * 4 + 128;
+  static constexpr int kBarOff = kQfOff + kQfBytes;
+  static constexpr int kMiscOff = kBarOff + kStages * 8;
+  static constexpr int kMiscBytes = 64 + kW * 4 + 2 * kRP * 4 + 128;
   static constexpr int kPreOff = kMiscOff + kMiscBytes;
   static __host__ __device__ constexpr int smem_bytes(int num_seqs) {
     return kPreOff + (2 * num_seqs + 1) * 4 + 1024;
   }
+  static_assert(kStages % kW == 0, "each ring stage must belong to one warp");
+  static_assert(kOBytes / 4 >= 1024, "the merge's slot list (<= 1024 blocks) must fit the O buffer");
 };
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+// Initial reference maximum of a row: finite, so exp2(score - ref) needs no
+// special case, and far below any score (the first page always raises it).
+constexpr float kNoScore = -1.0e30f;
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -315,10 +330,11 @@ __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
 // The kernel
 // ---------------------------------------------------------------------------
 template <int KVT, int NT>
-__global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, AttnCfg<KVT, NT>::kMinBlocks)
+__global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
     paged_attention_kernel(const __grid_constant__ CUtensorMap map, const AttnParams p) {
   using Cfg = AttnCfg<KVT, NT>;
-  constexpr int W = Cfg::kW, S = Cfg::kStages, RP = Cfg::kRP;
+  constexpr int W = Cfg::kW, S = Cfg::kStages, SPW = Cfg::kStagesPerWarp, RP = Cfg::kRP;
+  constexpr int nthr = W * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -328,22 +344,24 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, AttnCfg<KVT, NT>::
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + Cfg::kQOff);
   uint2* sQf = reinterpret_cast<uint2*>(smem + Cfg::kQfOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
-  uint64_t* empty = full + S;
   int* misc = reinterpret_cast<int*>(smem + Cfg::kMiscOff);
   volatile int* abort_flag = misc + 0;
-  int* merge_flag = misc + 1;
-  uint32_t* issued = reinterpret_cast<uint32_t*>(misc + 16);
-  uint32_t* consumed = issued + S;
-  float* sMrow = reinterpret_cast<float*>(consumed + S);
-  float* sLrow = sMrow + RP;
+  volatile int* merge_flag = misc + 1;
+  volatile int* has_frag = misc + 2;
+  float* sWarp = reinterpret_cast<float*>(misc + 16);          // [W] per-warp scratch
+  float* sMrow = sWarp + W;                                    // [RP]
+  float* sLrow = sMrow + RP;                                   // [RP]
+  FragIter* sit = reinterpret_cast<FragIter*>(sLrow + RP);
+  Frag* sf = reinterpret_cast<Frag*>(sit + 1);
   int* pre = reinterpret_cast<int*>(smem + Cfg::kPreOff);
   int* slen = pre + p.num_seqs + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
   const int B = p.num_seqs, H = p.num_kv_heads;
 
   // -- per-sequence lengths (clamped into the valid range) and page prefix
-  for (int s = tid; s < B; s += blockDim.x) {
+  for (int s = tid; s < B; s += nthr) {
     int L = p.seq_lens[s];
     const int Lmax = p.bt_stride * kPageSize;
     if (L < p.q_len || L > Lmax) {
@@ -356,12 +374,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, AttnCfg<KVT, NT>::
   if (tid == 0) {
     pre[0] = 0;
     misc[0] = 0;
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-      issued[i] = 0;
-      consumed[i] = 0;
-    }
+    for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -388,170 +401,204 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, AttnCfg<KVT, NT>::
   sp.C = gridDim.x;
   sp.k = p.num_splits;
 
-  if (warp == W) {
-    // ======================= producer warp =======================
-    if (lane == 0) prefetch_tensormap(&map);
-    const uint64_t policy = l2_evict_first_policy();
-    FragIter it;
-    it.init(sp, blockIdx.x);
-    Frag f;
-    uint32_t n = 0;
-    bool dead = false;
-    while (it.next(f)) {
-      const int* bt = p.block_table + (int64_t)f.s * p.bt_stride;
-      int nxt = (f.pg0 + lane < f.pg1) ? __ldg(bt + f.pg0 + lane) : 0;
-      for (int base = f.pg0; base < f.pg1; base += 32) {
-        const int id = nxt;
-        const int cnt = min(32, f.pg1 - base);
-        nxt = (base + 32 + lane < f.pg1) ? __ldg(bt + base + 32 + lane) : 0;
-        const bool bad = lane < cnt && (id < 0 || (int64_t)id >= p.num_pages);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, PQKV_DEV_PAGE_RANGE);
-        for (int j = 0; j < cnt; ++j, ++n) {
-          const int pid = __shfl_sync(0xffffffffu, id, j);
-          if (lane == 0 && !dead) {
-            const int stage = n % S;
-            const uint32_t round = n / S;
-            if (*abort_flag || !mbar_wait(&empty[stage], (round & 1) ^ 1)) {
-              dead = true;
-              *abort_flag = 1;
-              report(p.status, PQKV_DEV_TIMEOUT);
-            } else {
-              mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
-              tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, f.h, pid,
-                          policy);
-              issued[stage] += 1;
-            }
-          }
-        }
-      }
-    }
+  // -- this block's contiguous range [x0, x1) of the (page, kv-head) unit list
+  int64_t x0 = 0, x1 = 0;
+  if (sp.k == 0) {
+    x0 = sp.start(blockIdx.x);
+    x1 = sp.start(blockIdx.x + 1);
   } else {
-    // ======================= consumer warps =======================
-    const int g = lane >> 2, t = lane & 3;
-    const int nthr = W * 32;
-    const int ctid = tid;  // 0 .. W*32-1
-    // The four consumer warps walk the fragments in lock step; one copy of the
-    // iterator lives in shared memory and consumer thread 0 advances it.
-    FragIter* sit = reinterpret_cast<FragIter*>(sLrow + RP);
-    Frag* sf = reinterpret_cast<Frag*>(sit + 1);
-    volatile int* has_frag = merge_flag + 1;
-    if (ctid == 0) sit->init(sp, blockIdx.x);
-    uint32_t n0 = 0;
-    int cur_seg = -1, cur_L = 0;
-    QFrags<NT, Cfg::kQRegs> qf;
-    qf.tab = sQf;
-    float qk_scale = 0.f, v_mult = 1.f;
-    int lim[NT][2];
-    int lim_min = 0;
-    bool dead = false;
+    const int seg = blockIdx.x / sp.k, q = blockIdx.x % sp.k;
+    if (seg < B * H) {
+      const int s0 = seg / H, np = sp.pages(s0);
+      const int64_t a = (int64_t)pre[s0] * H + (int64_t)(seg % H) * np;
+      x0 = a + (int64_t)q * np / sp.k;
+      x1 = a + (int64_t)(q + 1) * np / sp.k;
+    }
+  }
+  const int ntot = (int)(x1 - x0);
 
-    for (;;) {
-      if (ctid == 0) *has_frag = sit->next(*sf) ? 1 : 0;
-      consumer_sync(nthr);
-      if (!*has_frag) break;
-      const int f_s = sf->s, f_h = sf->h, f_pg0 = sf->pg0, f_pg1 = sf->pg1, f_seg = sf->seg;
-      // ---- (re)load the query rows of this (sequence, kv-head)
-      if (f_seg != cur_seg) {
-        const int L = slen[f_s];
-        for (int v = ctid; v < RP * 16; v += nthr) {
-          const int r = v >> 4, c8 = v & 15;
-          uint4 val = make_uint4(0, 0, 0, 0);
-          if (r < p.rows) {
-            const int i = r / p.group, gh = r % p.group;
-            const int64_t row = ((int64_t)f_s * p.q_len + i) * p.num_q_heads + f_h * p.group + gh;
-            val = __ldg(reinterpret_cast<const uint4*>(p.q + row * kHeadDim) + c8);
-          }
-          reinterpret_cast<uint4*>(sQ)[v] = val;
+  // -- tile feed: warp w streams the block's pages w, w+W, w+2W, ... into its
+  //    own stages.  Its u-th page is i = w + u*W; lane l caches the kv-head
+  //    and pool page of the warp's pages u in [ubase, ubase+32) (cur) and the
+  //    next 32 (nxt).
+  const uint64_t policy = l2_evict_first_policy();
+  if (tid == 0) prefetch_tensormap(&map);
+  auto lookup = [&](int u, int& id, int& h) {
+    const int i = warp + u * W;
+    id = 0;
+    h = 0;
+    if (i >= ntot) return;
+    const int64_t x = x0 + i;
+    int lo = 0, hi = B - 1;                       // sequence holding unit x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)pre[mid] * H <= x) lo = mid; else hi = mid - 1;
+    }
+    const int np = pre[lo + 1] - pre[lo];
+    const int64_t off = x - (int64_t)pre[lo] * H;
+    h = (int)(off / np);
+    const int pg = (int)(off % np);
+    id = __ldg(p.block_table + (int64_t)lo * p.bt_stride + pg);
+    if (id < 0 || (int64_t)id >= p.num_pages) report(p.status, PQKV_DEV_PAGE_RANGE);
+  };
+  int cur_id, cur_h, nxt_id, nxt_h, ubase = 0;
+  lookup(lane, cur_id, cur_h);
+  lookup(32 + lane, nxt_id, nxt_h);
+  int issued_u = 0;                      // pages of this warp issued so far
+  auto issue_next = [&]() {
+    const int u = issued_u;
+    const int i = warp + u * W;
+    if (i >= ntot) return;
+    if (u - ubase >= 32) {
+      cur_id = nxt_id;
+      cur_h = nxt_h;
+      ubase += 32;
+      lookup(ubase + 32 + lane, nxt_id, nxt_h);
+    }
+    const int id = __shfl_sync(0xffffffffu, cur_id, u - ubase);
+    const int h = __shfl_sync(0xffffffffu, cur_h, u - ubase);
+    if (lane == 0) {
+      const int stage = i % S;
+      mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
+      tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, h, id, policy);
+    }
+    issued_u = u + 1;
+  };
+#pragma unroll 1
+  for (int k = 0; k < SPW; ++k) issue_next();
+
+  // -- walk the fragments of the block's range in lock step
+  if (tid == 0) sit->init(sp, blockIdx.x);
+  uint32_t n0 = 0;
+  int consumed_u = 0;
+  int cur_seg = -1, cur_L = 0;
+  QFrags<NT, Cfg::kQRegs> qf;
+  qf.tab = sQf;
+  float qk_scale = 0.f, v_mult = 1.f;
+  int lim[NT][2];
+  int lim_min = 0;
+  bool dead = false;
+
+  for (;;) {
+    if (tid == 0) *has_frag = sit->next(*sf) ? 1 : 0;
+    __syncthreads();
+    if (!*has_frag) break;
+    const int f_s = sf->s, f_h = sf->h, f_pg0 = sf->pg0, f_pg1 = sf->pg1, f_seg = sf->seg;
+    // ---- (re)load the query rows of this (sequence, kv-head)
+    if (f_seg != cur_seg) {
+      const int L = slen[f_s];
+      for (int v = tid; v < RP * 16; v += nthr) {
+        const int r = v >> 4, c8 = v & 15;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (r < p.rows) {
+          const int i = r / p.group, gh = r % p.group;
+          const int64_t row = ((int64_t)f_s * p.q_len + i) * p.num_q_heads + f_h * p.group + gh;
+          val = __ldg(reinterpret_cast<const uint4*>(p.q + row * kHeadDim) + c8);
         }
-        consumer_sync(nthr);
-        if (warp == 0) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int db = k_dim_base<KVT>(t, kk);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              sQf[(kk * NT + nt) * 32 + lane] =
-                  *reinterpret_cast<const uint2*>(sQ + (8 * nt + g) * kHeadDim + db);
-          }
-        }
-        const int sh = p.scale_per_head ? f_h : 0;
-        if (KVT == PQKV_KV_FP16) {
-          qk_scale = p.sm_scale_log2;
-          v_mult = 1.f;
-        } else {
-          const float ks = __ldg(p.k_scale + sh), vs = __ldg(p.v_scale + sh);
-          if (!(ks > 0.f && ks <= 3.4e38f && vs > 0.f && vs <= 3.4e38f))
-            report(p.status, PQKV_DEV_BAD_SCALE);
-          qk_scale = ks * p.sm_scale_log2;
-          v_mult = vs;
-        }
-        lim_min = L - p.q_len;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int r = 8 * nt + 2 * t + c;
-            lim[nt][c] = r < p.rows ? lim_min + r / p.group : 0x7fffffff;
-          }
-        cur_seg = f_seg;
-        cur_L = L;
-        consumer_sync(nthr);
+        reinterpret_cast<uint4*>(sQ)[v] = val;
       }
-
-      // ---- stream this warp's pages of the fragment
-      float o[8][NT][4];
-      float mref[NT][2], lsum[NT][2];
+      __syncthreads();
+      if (warp == 0) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+        for (int kk = 0; kk < 8; ++kk) {
+          const int db = k_dim_base<KVT>(t, kk);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            sQf[(kk * NT + nt) * 32 + lane] =
+                *reinterpret_cast<const uint2*>(sQ + (8 * nt + g) * kHeadDim + db);
+        }
+      }
+      const int sh = p.scale_per_head ? f_h : 0;
+      if (KVT == PQKV_KV_FP16) {
+        qk_scale = p.sm_scale_log2;
+        v_mult = 1.f;
+      } else {
+        const float ks = __ldg(p.k_scale + sh), vs = __ldg(p.v_scale + sh);
+        if (!(ks > 0.f && ks <= 3.4e38f && vs > 0.f && vs <= 3.4e38f))
+          report(p.status, PQKV_DEV_BAD_SCALE);
+        qk_scale = ks * p.sm_scale_log2;
+        v_mult = vs;
+      }
+      lim_min = L - p.q_len;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          mref[nt][c] = -INFINITY;
-          lsum[nt][c] = 0.f;
+          const int r = 8 * nt + 2 * t + c;
+          lim[nt][c] = r < p.rows ? lim_min + r / p.group : 0x7fffffff;
         }
+      cur_seg = f_seg;
+      cur_L = L;
+      __syncthreads();
+    }
+
+    // ---- stream this warp's pages of the fragment
+    float o[8][NT][4];
+    float mref[NT][2], lsum[NT][2];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+      for (int c = 0; c < 2; ++c) {
+        mref[nt][c] = kNoScore;
+        lsum[nt][c] = 0.f;
       }
-      const int npg = f_pg1 - f_pg0;
-      const int first = (int)((warp - (int)(n0 % W) + W) % W);
-      for (int j = first; j < npg; j += W) {
-        const uint32_t gi = n0 + j;
-        const int stage = gi % S;
-        if (!dead) {
-          if (*abort_flag || !mbar_wait(&full[stage], (gi / S) & 1)) {
-            dead = true;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+    }
+    const int npg = f_pg1 - f_pg0;
+    const int first = (int)((warp - (int)(n0 % W) + W) % W);
+    for (int j = first; j < npg; j += W) {
+      const uint32_t gi = n0 + j;
+      const int stage = gi % S;
+      if (!dead) {
+        bool ok = !*abort_flag && mbar_wait(&full[stage], (gi / S) & 1);
+        ok = __all_sync(0xffffffffu, ok);       // keep the warp's control flow uniform
+        if (!ok) {
+          dead = true;
+          if (lane == 0) {
             *abort_flag = 1;
             report(p.status, PQKV_DEV_TIMEOUT);
           }
         }
-        if (dead) continue;
-        const uint8_t* T = ring + stage * Cfg::kTileBytes;
-        const int pos0 = (f_pg0 + j) * kPageSize;
+      }
+      if (dead) continue;
+      const uint8_t* T = ring + stage * Cfg::kTileBytes;
+      const int pos0 = (f_pg0 + j) * kPageSize;
 
-        // S^T = K Q^T
-        float sc[NT][4];
+      // S^T = K Q^T
+      float sc[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-        page_qk<KVT, NT, Cfg::kQRegs>(T, g, t, lane, qf, sc);
-        // scale into log2 units and mask
-        const bool need_mask = pos0 + kPageSize - 1 > lim_min;
+        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+      page_qk<KVT, NT, Cfg::kQRegs>(T, g, t, lane, qf, sc);
+
+      // scores in log2 units; masked -> -inf
+      const bool need_mask = pos0 + kPageSize - 1 > lim_min;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x = sc[nt][e] * qk_scale;
-            if (need_mask) {
-              const int tok = pos0 + g + ((e & 2) ? 8 : 0);
-              if (tok > lim[nt][e & 1]) x = -INFINITY;
-            }
-            sc[nt][e] = x;
+        for (int e = 0; e < 4; ++e) {
+          float x = sc[nt][e] * qk_scale;
+          if (need_mask) {
+            const int tok = pos0 + g + ((e & 2) ? 8 : 0);
+            if (tok > lim[nt][e & 1]) x = -INFINITY;
           }
-        // page maximum per query row (uniform over the 8 lanes holding the row)
-        float pm[NT][2];
-        bool raise = false;
+          sc[nt][e] = x;
+        }
+      // The reference maximum of a row only moves when one of its scores
+      // exceeds it by more than 8 (probabilities then stay <= 2^8).  Each lane
+      // tests its own scores; only then does the warp form the exact page
+      // maximum across the 8 lanes that share a row and rescale.
+      bool raise = false;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          raise |= fmaxf(sc[nt][c], sc[nt][c + 2]) > mref[nt][c] + 8.f;
+      if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -560,193 +607,209 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, AttnCfg<KVT, NT>::
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-            pm[nt][c] = m;
-            raise |= m > mref[nt][c] + 8.f;
-          }
-        if (__any_sync(0xffffffffu, raise)) {
+            if (m > mref[nt][c] + 8.f) {
+              const float fct = ex2(mref[nt][c] - m);
+              mref[nt][c] = m;
+              lsum[nt][c] *= fct;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              if (pm[nt][c] > mref[nt][c] + 8.f) {
-                const float fct = ex2(mref[nt][c] - pm[nt][c]);
-                mref[nt][c] = pm[nt][c];
-                lsum[nt][c] *= fct;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                  o[mt][nt][c] *= fct;
-                  o[mt][nt][c + 2] *= fct;
-                }
+              for (int mt = 0; mt < 8; ++mt) {
+                o[mt][nt][c] *= fct;
+                o[mt][nt][c + 2] *= fct;
               }
             }
-        }
-        // probabilities (<= 2^8), row sums, and P^T -> B fragments
-        uint32_t pb[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float pr[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float mr = mref[nt][e & 1];
-            pr[e] = ex2(sc[nt][e] - (mr == -INFINITY ? 0.f : mr));
           }
-          lsum[nt][0] += pr[0] + pr[2];
-          lsum[nt][1] += pr[1] + pr[3];
-          pb[nt][0] = movmatrix_trans(pack_half2(pr[0], pr[1]));
-          pb[nt][1] = movmatrix_trans(pack_half2(pr[2], pr[3]));
-        }
-        // O^T += V^T P^T
-        {
-          const bool tail = pos0 + kPageSize > cur_L;
-          VMask vm;
-          vm.init(t, cur_L - pos0);
-          page_pv<KVT, NT>(T, g, t, pb, tail, vm, o);
-        }
-        __syncwarp();
-        if (lane == 0) {
-          consumed[stage] += 1;
-          mbar_arrive(&empty[stage]);
-        }
       }
-      n0 += npg;
-
-      // ---- combine the warps' states of this fragment
+      // probabilities (<= 2^8), row sums, and P^T -> B fragments
+      uint32_t pb[NT][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt) {
+        float pr[4];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float l = lsum[nt][c];
-          l += __shfl_xor_sync(0xffffffffu, l, 4);
-          l += __shfl_xor_sync(0xffffffffu, l, 8);
-          l += __shfl_xor_sync(0xffffffffu, l, 16);
-          const int r = 8 * nt + 2 * t + c;
-          if (g == 0) {
-            sML[(warp * 2 + 0) * RP + r] = mref[nt][c];
-            sML[(warp * 2 + 1) * RP + r] = l;
-          }
-          float* dst = sO + ((size_t)warp * RP + r) * kHeadDim + 16 * g;
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            *reinterpret_cast<float4*>(dst + 4 * k4) =
-                make_float4(o[2 * k4][nt][c], o[2 * k4][nt][c + 2], o[2 * k4 + 1][nt][c],
-                            o[2 * k4 + 1][nt][c + 2]);
-        }
-      consumer_sync(nthr);
-
-      const int cnt = sp.count(f_seg, sf->a, sf->b);
-      const int slot = sp.k > 0 ? (int)blockIdx.x : f_seg + (int)blockIdx.x;
-      const int64_t out_row0 = (int64_t)f_s * p.q_len;
+        for (int e = 0; e < 4; ++e) pr[e] = ex2(sc[nt][e] - mref[nt][e & 1]);
+        lsum[nt][0] += pr[0] + pr[2];
+        lsum[nt][1] += pr[1] + pr[3];
+        pb[nt][0] = movmatrix_trans(pack_half2(pr[0], pr[1]));
+        pb[nt][1] = movmatrix_trans(pack_half2(pr[2], pr[3]));
+      }
+      // O^T += V^T P^T
       {
-        const int d = ctid;  // one head dim per consumer thread
-        for (int r = 0; r < p.rows; ++r) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
-          float acc = 0.f, l = 0.f;
-#pragma unroll
-          for (int w = 0; w < W; ++w) {
-            const float mw = sML[(w * 2) * RP + r];
-            const float sc = mw == -INFINITY ? 0.f : ex2(mw - M);
-            acc += sc * sO[((size_t)w * RP + r) * kHeadDim + d];
-            l += sc * sML[(w * 2 + 1) * RP + r];
-          }
-          if (cnt == 1) {
-            const int i = r / p.group, gh = r % p.group;
-            const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
-            const float val = l > 0.f ? acc / l * v_mult : 0.f;
-            p.out[orow * kHeadDim + d] = __half_as_ushort(__float2half_rn(val));
-          } else {
-            p.part_o[((size_t)slot * RP + r) * kHeadDim + d] = acc;
-            if (d == 0) {
-              p.part_ml[(size_t)slot * 2 * RP + r] = M;
-              p.part_ml[(size_t)slot * 2 * RP + RP + r] = l;
-            }
-          }
-        }
+        const bool tail = pos0 + kPageSize > cur_L;
+        VMask vm;
+        vm.init(t, cur_L - pos0);
+        page_pv<KVT, NT>(T, g, t, pb, tail, vm, o);
       }
-      if (cnt > 1) {
-        __threadfence();
-        consumer_sync(nthr);
-        if (ctid == 0) {
-          const int ticket = atomicAdd(p.counters + f_seg, 1);
-          *merge_flag = (ticket == cnt - 1);
-        }
-        consumer_sync(nthr);
-        if (*merge_flag) {
-          __threadfence();
-          // gather the segment's partial slots (fixed order) into shared memory
-          int* slots = reinterpret_cast<int*>(sO);
-          if (ctid == 0) {
-            int nsl = 0;
-            if (sp.k > 0) {
-              const int np = sp.pages(f_s);
-              for (int q = 0; q < sp.k; ++q)
-                if ((int64_t)(q + 1) * np / sp.k > (int64_t)q * np / sp.k)
-                  slots[nsl++] = f_seg * sp.k + q;
-            } else {
-              for (int64_t x = sf->a; x < sf->b;) {
-                const int cc = sp.cta_of(x);
-                slots[nsl++] = f_seg + cc;
-                x = sp.start(cc + 1);
-              }
-            }
-          }
-          consumer_sync(nthr);
-          // per-row maximum and normaliser
-          if (ctid < p.rows) {
-            const int r = ctid;
-            float M = -INFINITY;
-            for (int q = 0; q < cnt; ++q)
-              M = fmaxf(M, __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + r));
-            float l = 0.f;
-            for (int q = 0; q < cnt; ++q) {
-              const float mq = __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + r);
-              if (mq != -INFINITY)
-                l += ex2(mq - M) * __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + RP + r);
-            }
-            sMrow[r] = M;
-            sLrow[r] = l;
-          }
-          consumer_sync(nthr);
-          const int dq = ctid & 31, rg = ctid >> 5;
-          for (int r = rg; r < p.rows; r += W) {
-            const float M = sMrow[r];
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int q = 0; q < cnt; ++q) {
-              const size_t sl = slots[q];
-              const float mq = __ldcg(p.part_ml + sl * 2 * RP + r);
-              const float wq = mq == -INFINITY ? 0.f : ex2(mq - M);
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                          p.part_o + (sl * RP + r) * kHeadDim) +
-                                      dq);
-              acc.x += wq * v.x;
-              acc.y += wq * v.y;
-              acc.z += wq * v.z;
-              acc.w += wq * v.w;
-            }
-            const float inv = sLrow[r] > 0.f ? v_mult / sLrow[r] : 0.f;
-            const int i = r / p.group, gh = r % p.group;
-            const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
-            __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
-            __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
-            uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t*>(&h01);
-            pk.y = *reinterpret_cast<uint32_t*>(&h23);
-            *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
-          }
-          if (ctid == 0) p.counters[f_seg] = 0;
-        }
-      }
-      consumer_sync(nthr);
+      // the stage is free again: refill it with this warp's page S ahead
+      __syncwarp();
+      fence_proxy_async_smem();
+      consumed_u += 1;
+      issue_next();
     }
+    n0 += npg;
+
+    // ---- combine the warps' states of this fragment: every warp publishes
+    // its (m, l) per row, then the warps add their rescaled O into one shared
+    // buffer in warp order (deterministic, one warp-sized buffer)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float l = lsum[nt][c];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (g == 0) {
+          const int r = 8 * nt + 2 * t + c;
+          sML[(warp * 2 + 0) * RP + r] = mref[nt][c];
+          sML[(warp * 2 + 1) * RP + r] = l;
+        }
+      }
+    __syncthreads();
+    float fw[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int r = 8 * nt + 2 * t + c;
+        float M = sML[r];
+#pragma unroll
+        for (int w = 1; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
+        fw[nt][c] = ex2(mref[nt][c] - M);
+      }
+#pragma unroll 1
+    for (int w = 0; w < W; ++w) {
+      if (warp == w) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int r = 8 * nt + 2 * t + c;
+            float4* dst = reinterpret_cast<float4*>(sO + (size_t)r * kHeadDim + 16 * g);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              float4 v = make_float4(o[2 * k4][nt][c] * fw[nt][c], o[2 * k4][nt][c + 2] * fw[nt][c],
+                                     o[2 * k4 + 1][nt][c] * fw[nt][c],
+                                     o[2 * k4 + 1][nt][c + 2] * fw[nt][c]);
+              if (w > 0) {
+                const float4 u4 = dst[k4];
+                v.x += u4.x;
+                v.y += u4.y;
+                v.z += u4.z;
+                v.w += u4.w;
+              }
+              dst[k4] = v;
+            }
+          }
+      }
+      __syncthreads();
+    }
+
+    const int cnt = sp.count(f_seg, sf->a, sf->b);
+    const int slot = sp.k > 0 ? (int)blockIdx.x : f_seg + (int)blockIdx.x;
+    const int64_t out_row0 = (int64_t)f_s * p.q_len;
+    for (int idx = tid; idx < p.rows * kHeadDim; idx += nthr) {
+      const int r = idx / kHeadDim, d = idx % kHeadDim;
+      float M = sML[r];
+#pragma unroll
+      for (int w = 1; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
+      float l = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) l += ex2(sML[(w * 2) * RP + r] - M) * sML[(w * 2 + 1) * RP + r];
+      const float acc = sO[(size_t)r * kHeadDim + d];
+      if (cnt == 1) {
+        const int i = r / p.group, gh = r % p.group;
+        const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+        const float val = l > 0.f ? acc / l * v_mult : 0.f;
+        p.out[orow * kHeadDim + d] = __half_as_ushort(__float2half_rn(val));
+      } else {
+        p.part_o[((size_t)slot * RP + r) * kHeadDim + d] = acc;
+        if (d == 0) {
+          p.part_ml[(size_t)slot * 2 * RP + r] = M;
+          p.part_ml[(size_t)slot * 2 * RP + RP + r] = l;
+        }
+      }
+    }
+    if (cnt > 1) {
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int ticket = atomicAdd(p.counters + f_seg, 1);
+        *merge_flag = (ticket == cnt - 1);
+      }
+      __syncthreads();
+      if (*merge_flag) {
+        __threadfence();
+        // gather the segment's partial slots (fixed order) into shared memory
+        int* slots = reinterpret_cast<int*>(sO);
+        if (tid == 0) {
+          int nsl = 0;
+          if (sp.k > 0) {
+            const int np = sp.pages(f_s);
+            for (int q = 0; q < sp.k; ++q)
+              if ((int64_t)(q + 1) * np / sp.k > (int64_t)q * np / sp.k)
+                slots[nsl++] = f_seg * sp.k + q;
+          } else {
+            for (int64_t x = sf->a; x < sf->b;) {
+              const int cc = sp.cta_of(x);
+              slots[nsl++] = f_seg + cc;
+              x = sp.start(cc + 1);
+            }
+          }
+        }
+        __syncthreads();
+        // per-row maximum and normaliser
+        if (tid < p.rows) {
+          const int r = tid;
+          float M = kNoScore;
+          for (int q = 0; q < cnt; ++q)
+            M = fmaxf(M, __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + r));
+          float l = 0.f;
+          for (int q = 0; q < cnt; ++q) {
+            const float mq = __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + r);
+            l += ex2(mq - M) * __ldcg(p.part_ml + (size_t)slots[q] * 2 * RP + RP + r);
+          }
+          sMrow[r] = M;
+          sLrow[r] = l;
+        }
+        __syncthreads();
+        const int dq = lane, rg = warp;
+        for (int r = rg; r < p.rows; r += W) {
+          const float M = sMrow[r];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int q = 0; q < cnt; ++q) {
+            const size_t sl = slots[q];
+            const float wq = ex2(__ldcg(p.part_ml + sl * 2 * RP + r) - M);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                        p.part_o + (sl * RP + r) * kHeadDim) +
+                                    dq);
+            acc.x += wq * v.x;
+            acc.y += wq * v.y;
+            acc.z += wq * v.z;
+            acc.w += wq * v.w;
+          }
+          const float inv = sLrow[r] > 0.f ? v_mult / sLrow[r] : 0.f;
+          const int i = r / p.group, gh = r % p.group;
+          const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+          __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
+          __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&h01);
+          pk.y = *reinterpret_cast<uint32_t*>(&h23);
+          *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+        }
+        if (tid == 0) p.counters[f_seg] = 0;
+      }
+    }
+    __syncthreads();
   }
 
-  // ---- drain: never leave with a tile copy in flight
-  __syncthreads();
-  if (tid == 0 && *abort_flag) {
-    for (int i = 0; i < S; ++i)
-      if (issued[i] > consumed[i]) (void)mbar_wait(&full[i], (issued[i] - 1) & 1);
+  // ---- drain: never leave with a tile copy in flight (only after a timeout
+  //      can this warp have issued pages it did not consume)
+  if (lane == 0 && *abort_flag) {
+    for (int u = consumed_u; u < issued_u; ++u) {
+      const int i = warp + u * W;
+      (void)mbar_wait(&full[i % S], (i / S) & 1);
+    }
   }
 }
 

@@ -144,10 +144,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes_low16) {
   return r;
 }
 
-// E4M3: 4 codes of a word -> (d0,d1), (d2,d3)
+// E4M3: 4 codes of a word -> (d0,d1), (d2,d3); the halves of the word feed
+// the conversions directly
 __device__ __forceinline__ void e4m3_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  lo = e4m3x2_to_f16x2(w);
-  hi = e4m3x2_to_f16x2(w >> 16);
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // INT8: code c becomes the fp16 1024 + (c + 128) by placing (c ^ 0x80) under
