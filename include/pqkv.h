@@ -174,6 +174,41 @@ int pqkv_paged_attention(const void* q, void* out, const void* pages, int64_t nu
                          int32_t max_seq_len, void* workspace, size_t workspace_bytes,
                          int32_t* status, void* stream);
 
+/* Size of the library-owned scratch area used by pqkv_paged_attention_noalloc
+ * (16 MiB, held on every GPU that loads the library until the process exits). */
+#define PQKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * pqkv_paged_attention_noalloc -- pqkv_paged_attention for callers that cannot
+ * allocate device memory.  (No counterpart on the ReVolta pages: an addition of
+ * this library for callers such as runtimes that budget all device memory up
+ * front and forbid cudaMalloc at call time, hooks running inside another
+ * framework's step that must not bypass its allocator, or C callers with no
+ * allocator at all.)
+ *
+ * Same arguments and result as pqkv_paged_attention without the workspace:
+ * the library uses its own fixed scratch area of PQKV_NOALLOC_SCRATCH_BYTES, a
+ * file-scope device array.  Nothing is allocated or freed, by the library or by
+ * any routine it calls.
+ *   - Returns PQKV_ERANGE when pqkv_paged_attention_workspace_size() for these
+ *     sizes exceeds PQKV_NOALLOC_SCRATCH_BYTES (num_splits == 1 needs none).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call on a device shares the one scratch area and it keeps the last
+ *     call's contents; each call clears the part that must start at zero
+ *     (cudaMemsetAsync on `stream`).  Calls that overlap on the GPU (different
+ *     streams, or concurrent host threads) race on it and must be serialised by
+ *     the caller.
+ */
+int pqkv_paged_attention_noalloc(const void* q, void* out, const void* pages, int64_t num_pages,
+                                 const int32_t* block_table, int32_t max_pages_per_seq,
+                                 const int32_t* seq_lens, int32_t num_seqs, int32_t q_len,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t page_size, int32_t kv_dtype, const float* k_scale,
+                                 const float* v_scale, int32_t scale_per_head, int32_t num_splits,
+                                 int32_t max_seq_len, int32_t* status, void* stream);
+
 /* Bytes at the start of the workspace that hold merge counters. */
 #define PQKV_COUNTER_BYTES(num_seqs, num_kv_heads) \
   ((((size_t)(num_seqs) * (size_t)(num_kv_heads) * 4u) + 255u) & ~(size_t)255u)

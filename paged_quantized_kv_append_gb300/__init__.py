@@ -66,6 +66,11 @@ def load_library(path: str | None = None):
         lib.pqkv_paged_attention.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_vp, c_i32,
                                              c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
                                              c_i32, c_i32, c_i32, c_vp, c_sz, c_vp, c_vp]
+        lib.pqkv_paged_attention_noalloc.restype = ctypes.c_int
+        lib.pqkv_paged_attention_noalloc.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_vp,
+                                                     c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                                     c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp,
+                                                     c_vp]
         lib.pqkv_status_string.restype = ctypes.c_char_p
         lib.pqkv_status_string.argtypes = [ctypes.c_int]
         lib.pqkv_version.restype = ctypes.c_char_p
@@ -227,6 +232,45 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
         _ptr(k_scale if kd != FP16 else None), _ptr(v_scale if kd != FP16 else None), sph,
         num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_attention_noalloc(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v_scale,
+                            out, num_splits=0, max_seq_len=0, status=None, stream=None):
+    """paged_attention for callers that cannot allocate device memory: the
+    library uses its own fixed 16 MiB scratch area instead of a workspace.
+
+    The first call on a device must come before any stream capture; calls on
+    one device share the scratch area and must not overlap on the GPU.
+    Raises ValueError when the sizes need more scratch than the area holds.
+    """
+    kd = _dtype_id(kv_dtype)
+    _check_pages(pages, kd)
+    H = pages.shape[1]
+    if q.dtype != torch.float16 or q.dim() != 3 or q.shape[2] != HEAD_DIM or not q.is_contiguous():
+        raise ValueError("q must be contiguous fp16 [num_seqs*q_len, Hq, 128]")
+    if out.shape != q.shape or out.dtype != torch.float16 or not out.is_contiguous():
+        raise ValueError("out must be contiguous fp16 shaped like q")
+    B = seq_lens.shape[0]
+    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32 or \
+            block_table.shape[0] != B or not block_table.is_contiguous():
+        raise ValueError("seq_lens / block_table must be int32 with one row per sequence")
+    if q.shape[0] != B * q_len:
+        raise ValueError("q has %d rows, expected num_seqs*q_len = %d" % (q.shape[0], B * q_len))
+    sph = 0
+    if kd != FP16:
+        sph = _check_scale(k_scale, H, "k_scale")
+        if _check_scale(v_scale, H, "v_scale") != sph:
+            raise ValueError("k_scale and v_scale must have the same shape")
+    rc = load_library().pqkv_paged_attention_noalloc(
+        _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), B, q_len, q.shape[1], H, HEAD_DIM, PAGE_SIZE, kd,
+        _ptr(k_scale if kd != FP16 else None), _ptr(v_scale if kd != FP16 else None), sph,
+        num_splits, max_seq_len, _ptr(status), _stream(q, stream))
+    _check(rc, "paged_attention_noalloc")
     return out
 
 

@@ -1,0 +1,59 @@
+"""pqkv_paged_attention_noalloc: attention for callers that cannot allocate
+device memory (for example a runtime that budgets all GPU memory up front and
+forbids cudaMalloc at call time).  It must give the same result as
+pqkv_paged_attention with a caller workspace, call after call, although its
+scratch area keeps the previous call's contents.
+
+Kept in a file of its own that is collected after every other test file.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.helpers import Case, assert_close, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(pq, c, out, num_splits=0):
+    w = c.w
+    return pq.paged_attention_noalloc(c.q, c.pages, c.bt, c.seq_lens, w.q_len, w.kv_dtype, c.ks,
+                                      c.vs, out, num_splits=num_splits)
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_noalloc_matches_workspace_entry_point_twice(num_splits):
+    pq = require_gpu()
+    c = Case(W.workload("e4m3_verify_512k_stress", scale=0.004), with_oracle=False)
+    ref = c.attention(num_splits=num_splits)          # existing entry point, caller workspace
+    ref64 = ref.float().cpu().numpy().astype(np.float64)
+    for call in range(2):                            # the scratch keeps the last call's contents
+        out = torch.full_like(c.q, float("nan"))
+        _noalloc(pq, c, out, num_splits)
+        torch.cuda.synchronize()
+        assert_close(out, ref64, "noalloc call %d splits %d" % (call, num_splits))
+
+
+def test_noalloc_int8_decode_and_no_split():
+    pq = require_gpu()
+    c = Case(W.workload("int8_decode_append_262k", scale=0.004), with_oracle=False)
+    for ns in (0, 1):
+        ref = c.attention(num_splits=ns).float().cpu().numpy().astype(np.float64)
+        out = torch.empty_like(c.q)
+        _noalloc(pq, c, out, ns)
+        assert_close(out, ref, "noalloc int8 splits %d" % ns)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    pq = require_gpu()
+    # 2048 sequences x 8 kv-heads in the balanced split need more than 16 MiB
+    B, H, q_len, Hq = 2048, 8, 5, 32
+    assert pq.workspace_size(B, q_len, Hq, H) > pq.NOALLOC_SCRATCH_BYTES
+    q = torch.zeros((B * q_len, Hq, 128), dtype=torch.float16, device="cuda")
+    pages = pq.new_pages(4, H, W.FP8_E4M3, "cuda", fill=0)
+    bt = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
+    sl = torch.full((B,), 5, dtype=torch.int32, device="cuda")
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        pq.paged_attention_noalloc(q, pages, bt, sl, q_len, W.FP8_E4M3, one, one, torch.empty_like(q))
