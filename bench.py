@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pqkv", "reference"], default="pqkv")
     ap.add_argument("--workload", default="e4m3_verify_512k_stress")
@@ -88,9 +88,12 @@ def max_over_ranks(x: float, world: int) -> float:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms; only those taken inside the timed
+    region (by their own timestamps) enter the summary."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
@@ -103,36 +106,49 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    @classmethod
+    def summarize(cls, path, t_start, t_end):
+        import datetime as dt
+        sm, smax, reasons, total = [], None, set(), 0
+        for line in open(path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                mhz, mx = float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            total += 1
+            smax = mx
+            if not (t_start <= ts <= t_end):
+                continue
+            sm.append(mhz)
+            for n, v in zip(cls.REASONS, f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples_in_timed_region": len(sm),
+                "samples_total": total}
+
+    def stop(self, t_start, t_end):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+        r = self.summarize(self.path, t_start, t_end)
+        r["window_s"] = round(t_end - t_start, 4)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return r
 
 
 # ---------------------------------------------------------------------------
@@ -324,13 +340,15 @@ def run_pqkv(args, rank, local, world):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    w_start = time.time()
     t0.record(stream)
     for i in range(args.steps):
         step(attn_ev[i])
     t1.record(stream)
     torch.cuda.synchronize()
+    w_end = time.time()
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop(w_start, w_end)
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = total_ms / args.steps
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
