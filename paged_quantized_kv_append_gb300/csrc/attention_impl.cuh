@@ -55,7 +55,6 @@ struct AttnCfg {
   static constexpr int kStagesPerWarp = (KVT == PQKV_KV_FP16) ? 2 : (kW <= 8 ? 4 : 3);
   static constexpr int kStages = kW * kStagesPerWarp;
   static constexpr int kRP = 8 * NT;                               // padded query rows
-  static constexpr bool kQRegs = false;     // Q fragments live in a shared table
   static constexpr int kQfBytes = 8 * NT * 32 * 8;
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kRingOff = 0;
@@ -189,20 +188,14 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* base, int line, int chunk
   return *reinterpret_cast<const uint4*>(base + line * 128 + ((chunk ^ (line & 7)) << 4));
 }
 
-// Source of the Q^T B-fragments: registers (N <= 16) or a shared table.
-template <int NT, bool kRegs>
+// The Q^T B-fragments live in a shared table [4][NT][32] of 16-byte entries:
+// a lane's fragments of k-steps 2*k2 and 2*k2 + 1 of one row tile side by
+// side, so one 16-byte load serves two k-steps.
+template <int NT>
 struct QFrags {
-  uint32_t r[kRegs ? 8 : 1][NT][2];
-  const uint2* tab;   // [8][NT][32] when !kRegs
-  __device__ __forceinline__ void get(int kk, int nt, int lane, uint32_t& b0, uint32_t& b1) const {
-    if (kRegs) {
-      b0 = r[kRegs ? kk : 0][nt][0];
-      b1 = r[kRegs ? kk : 0][nt][1];
-    } else {
-      const uint2 q = tab[(kk * NT + nt) * 32 + lane];
-      b0 = q.x;
-      b1 = q.y;
-    }
+  const uint4* tab;
+  __device__ __forceinline__ uint4 get2(int k2, int nt, int lane) const {
+    return tab[(k2 * NT + nt) * 32 + lane];
   }
 };
 
@@ -215,9 +208,9 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t& lo, uint32_t&
 // S^T[16 tokens][8*NT rows] = K Q^T for one page tile.  Lane (g, t) feeds the
 // K rows of tokens g and g+8 and gets back S^T for tokens (g, g+8) and query
 // rows (8nt + 2t, 8nt + 2t + 1).  Codes are widened just before each k-step.
-template <int KVT, int NT, bool kRegs>
+template <int KVT, int NT>
 __device__ __forceinline__ void page_qk(const uint8_t* T, int g, int t, int lane,
-                                        const QFrags<NT, kRegs>& qf, float (&sc)[NT][4]) {
+                                        const QFrags<NT>& qf, float (&sc)[NT][4]) {
   if (KVT == PQKV_KV_FP16) {
     const int c1 = (t & 1) | ((t & 2) << 1);
 #pragma unroll
@@ -227,11 +220,9 @@ __device__ __forceinline__ void page_qk(const uint8_t* T, int g, int t, int lane
       const uint4 y = lds128(T, 2 * (g + 8) + lh, ch);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        uint32_t b0, b1;
-        qf.get(2 * q, nt, lane, b0, b1);
-        mma_16816(sc[nt], x.x, y.x, x.y, y.y, b0, b1);
-        qf.get(2 * q + 1, nt, lane, b0, b1);
-        mma_16816(sc[nt], x.z, y.z, x.w, y.w, b0, b1);
+        const uint4 b = qf.get2(q, nt, lane);
+        mma_16816(sc[nt], x.x, y.x, x.y, y.y, b.x, b.y);
+        mma_16816(sc[nt], x.z, y.z, x.w, y.w, b.z, b.w);
       }
     }
   } else {
@@ -240,15 +231,19 @@ __device__ __forceinline__ void page_qk(const uint8_t* T, int g, int t, int lane
       const uint4 x = lds128(T, g, 2 * t + half), y = lds128(T, g + 8, 2 * t + half);
       const uint32_t wx[4] = {x.x, x.y, x.z, x.w}, wy[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t a0, a1, a2, a3;
-        dequant_word<KVT>(wx[j], a0, a2);
-        dequant_word<KVT>(wy[j], a1, a3);
+      for (int j2 = 0; j2 < 2; ++j2) {
+        uint4 b[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          uint32_t b0, b1;
-          qf.get(4 * half + j, nt, lane, b0, b1);
-          mma_16816(sc[nt], a0, a1, a2, a3, b0, b1);
+        for (int nt = 0; nt < NT; ++nt) b[nt] = qf.get2(2 * half + j2, nt, lane);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * j2 + jj;
+          uint32_t a0, a1, a2, a3;
+          dequant_word<KVT>(wx[j], a0, a2);
+          dequant_word<KVT>(wy[j], a1, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816(sc[nt], a0, a1, a2, a3, jj ? b[nt].z : b[nt].x, jj ? b[nt].w : b[nt].y);
         }
       }
     }
@@ -306,14 +301,14 @@ __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       if (KVT == PQKV_KV_FP8_E4M3) {
-        const uint32_t ab_lo = __byte_perm(a[wi], b[wi], 0x5140);
-        const uint32_t cd_lo = __byte_perm(c[wi], d[wi], 0x5140);
-        mma_mt(2 * wi, e4m3x2_to_f16x2(ab_lo), e4m3x2_to_f16x2(ab_lo >> 16),
-               e4m3x2_to_f16x2(cd_lo), e4m3x2_to_f16x2(cd_lo >> 16));
-        const uint32_t ab_hi = __byte_perm(a[wi], b[wi], 0x7362);
-        const uint32_t cd_hi = __byte_perm(c[wi], d[wi], 0x7362);
-        mma_mt(2 * wi + 1, e4m3x2_to_f16x2(ab_hi), e4m3x2_to_f16x2(ab_hi >> 16),
-               e4m3x2_to_f16x2(cd_hi), e4m3x2_to_f16x2(cd_hi >> 16));
+        // the two halves of each interleaved word feed the conversions directly
+        uint32_t x0, x1, x2, x3;
+        e4m3_word(__byte_perm(a[wi], b[wi], 0x5140), x0, x1);
+        e4m3_word(__byte_perm(c[wi], d[wi], 0x5140), x2, x3);
+        mma_mt(2 * wi, x0, x1, x2, x3);
+        e4m3_word(__byte_perm(a[wi], b[wi], 0x7362), x0, x1);
+        e4m3_word(__byte_perm(c[wi], d[wi], 0x7362), x2, x3);
+        mma_mt(2 * wi + 1, x0, x1, x2, x3);
       } else {
         mma_mt(2 * wi, i8pair(__byte_perm(a[wi], b[wi], 0x0400)),
                i8pair(__byte_perm(a[wi], b[wi], 0x0501)), i8pair(__byte_perm(c[wi], d[wi], 0x0400)),
@@ -342,7 +337,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   float* sO = reinterpret_cast<float*>(smem + Cfg::kOOff);
   float* sML = reinterpret_cast<float*>(smem + Cfg::kMLOff);
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + Cfg::kQOff);
-  uint2* sQf = reinterpret_cast<uint2*>(smem + Cfg::kQfOff);
+  uint4* sQf = reinterpret_cast<uint4*>(smem + Cfg::kQfOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
   int* misc = reinterpret_cast<int*>(smem + Cfg::kMiscOff);
   volatile int* abort_flag = misc + 0;
@@ -472,9 +467,9 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   uint32_t n0 = 0;
   int consumed_u = 0;
   int cur_seg = -1, cur_L = 0;
-  QFrags<NT, Cfg::kQRegs> qf;
+  QFrags<NT> qf;
   qf.tab = sQf;
-  float qk_scale = 0.f, v_mult = 1.f;
+  float qk_scale = 0.f, inv_qk_scale = 0.f, v_mult = 1.f;
   int lim[NT][2];
   int lim_min = 0;
   bool dead = false;
@@ -504,7 +499,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
           const int db = k_dim_base<KVT>(t, kk);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            sQf[(kk * NT + nt) * 32 + lane] =
+            reinterpret_cast<uint2*>(sQf)[(((kk >> 1) * NT + nt) * 32 + lane) * 2 + (kk & 1)] =
                 *reinterpret_cast<const uint2*>(sQ + (8 * nt + g) * kHeadDim + db);
         }
       }
@@ -519,6 +514,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         qk_scale = ks * p.sm_scale_log2;
         v_mult = vs;
       }
+      inv_qk_scale = 1.f / qk_scale;
       lim_min = L - p.q_len;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -534,12 +530,13 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
 
     // ---- stream this warp's pages of the fragment
     float o[8][NT][4];
-    float mref[NT][2], lsum[NT][2];
+    float mref[NT][2], lsum[NT][2], thr[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         mref[nt][c] = kNoScore;
+        thr[nt][c] = (kNoScore + 8.f) * inv_qk_scale;
         lsum[nt][c] = 0.f;
       }
 #pragma unroll
@@ -573,31 +570,28 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-      page_qk<KVT, NT, Cfg::kQRegs>(T, g, t, lane, qf, sc);
+      page_qk<KVT, NT>(T, g, t, lane, qf, sc);
 
-      // scores in log2 units; masked -> -inf
-      const bool need_mask = pos0 + kPageSize - 1 > lim_min;
+      // Raw scores; masked -> -inf.  The log2-domain score is sc * qk_scale.
+      if (pos0 + kPageSize - 1 > lim_min) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x = sc[nt][e] * qk_scale;
-          if (need_mask) {
+          for (int e = 0; e < 4; ++e) {
             const int tok = pos0 + g + ((e & 2) ? 8 : 0);
-            if (tok > lim[nt][e & 1]) x = -INFINITY;
+            if (tok > lim[nt][e & 1]) sc[nt][e] = -INFINITY;
           }
-          sc[nt][e] = x;
-        }
+      }
       // The reference maximum of a row only moves when one of its scores
       // exceeds it by more than 8 (probabilities then stay <= 2^8).  Each lane
-      // tests its own scores; only then does the warp form the exact page
-      // maximum across the 8 lanes that share a row and rescale.
+      // tests its own raw scores against thr = (mref + 8) / qk_scale; only
+      // then does the warp form the exact page maximum across the 8 lanes
+      // that share a row and rescale.
       bool raise = false;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          raise |= fmaxf(sc[nt][c], sc[nt][c + 2]) > mref[nt][c] + 8.f;
+        for (int c = 0; c < 2; ++c) raise |= fmaxf(sc[nt][c], sc[nt][c + 2]) > thr[nt][c];
       if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -607,9 +601,11 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            m *= qk_scale;
             if (m > mref[nt][c] + 8.f) {
               const float fct = ex2(mref[nt][c] - m);
               mref[nt][c] = m;
+              thr[nt][c] = (m + 8.f) * inv_qk_scale;
               lsum[nt][c] *= fct;
 #pragma unroll
               for (int mt = 0; mt < 8; ++mt) {
@@ -625,7 +621,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
       for (int nt = 0; nt < NT; ++nt) {
         float pr[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pr[e] = ex2(sc[nt][e] - mref[nt][e & 1]);
+        for (int e = 0; e < 4; ++e) pr[e] = ex2(fmaf(sc[nt][e], qk_scale, -mref[nt][e & 1]));
         lsum[nt][0] += pr[0] + pr[2];
         lsum[nt][1] += pr[1] + pr[3];
         pb[nt][0] = movmatrix_trans(pack_half2(pr[0], pr[1]));

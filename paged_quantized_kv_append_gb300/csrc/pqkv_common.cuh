@@ -135,15 +135,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // 8-bit code -> fp16 conversions (exact: every E4M3 value and every integer
 // in [-127, 127] is an fp16 value)
 // ---------------------------------------------------------------------------
-// two E4M3 codes (low byte -> low half) to an f16x2
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes_low16) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-      : "=r"(r)
-      : "r"(two_codes_low16));
-  return r;
-}
-
 // E4M3: 4 codes of a word -> (d0,d1), (d2,d3); the halves of the word feed
 // the conversions directly
 __device__ __forceinline__ void e4m3_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
