@@ -47,6 +47,8 @@ def parse_args():
                          "smaller values are for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay timing of the same step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -356,6 +358,33 @@ def run_pqkv(args, rank, local, world):
     step_bytes = attn_bytes + app_bytes
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
 
+    # ---- the same step captured once in a CUDA graph and replayed
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        g_ms = max_over_ranks(g0.elapsed_time(g1), world) / args.steps
+        graph = {"value": world * (attn_bytes + app_bytes) / (g_ms * 1e-3) / 1e9, "unit": UNIT,
+                 "us_per_step": g_ms * 1e3, "launches_per_step": launches_per_step}
+        del g
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -421,6 +450,7 @@ def run_pqkv(args, rank, local, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
+        "graph": graph,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(args.workload, args.cpu_seconds)

@@ -52,15 +52,21 @@ struct AttnCfg {
   static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
   static constexpr int kTileBytes = kLines * 128;
-  static constexpr int kStagesPerWarp = (KVT == PQKV_KV_FP16) ? 2 : (kW <= 8 ? 4 : 3);
+  static constexpr int kStagesPerWarp =
+      (KVT == PQKV_KV_FP16) ? 2 : (kW <= 8 ? 4 : (kW == 12 ? 3 : 2));
   static constexpr int kStages = kW * kStagesPerWarp;
   static constexpr int kRP = 8 * NT;                               // padded query rows
   static constexpr int kQfBytes = 8 * NT * 32 * 8;
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kRingOff = 0;
   static constexpr int kOOff = kRingOff + kStages * kTileBytes;
-  static constexpr int kOBytes = kRP * kHeadDim * 4;     // one warp's O, summed in turn
-  static constexpr int kMLOff = kOOff + kOBytes;
+  // With 12 or 16 warps the warps' O are combined in groups of four (warp w
+  // into buffer w / 4, in turn inside the group), then the group buffers are
+  // added in fixed order; 8 warps take turns on one buffer.
+  static constexpr int kCombGroups = kW >= 12 ? kW / 4 : 1;
+  static constexpr int kCombSize = kW / kCombGroups;
+  static constexpr int kOBytes = kRP * kHeadDim * 4;     // one group buffer
+  static constexpr int kMLOff = kOOff + kCombGroups * kOBytes;
   static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
   static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
   static constexpr int kBarOff = kQfOff + kQfBytes;
@@ -71,6 +77,7 @@ struct AttnCfg {
     return kPreOff + (2 * num_seqs + 1) * 4 + 1024;
   }
   static_assert(kStages % kW == 0, "each ring stage must belong to one warp");
+  static_assert(kW % kCombGroups == 0, "whole combine groups");
   static_assert(kOBytes / 4 >= 1024, "the merge's slot list (<= 1024 blocks) must fit the O buffer");
 };
 
@@ -643,8 +650,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
     n0 += npg;
 
     // ---- combine the warps' states of this fragment: every warp publishes
-    // its (m, l) per row, then the warps add their rescaled O into one shared
-    // buffer in warp order (deterministic, one warp-sized buffer)
+    // its (m, l) per row, then the warps add their rescaled O into their
+    // group's shared buffer, the members of a group in turn (all groups at
+    // once); the output step adds the group buffers in order.  Fixed order
+    // throughout, so the result is deterministic.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -671,15 +680,18 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         for (int w = 1; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
         fw[nt][c] = ex2(mref[nt][c] - M);
       }
+    const int comb_group = Cfg::kCombGroups > 1 ? warp / Cfg::kCombSize : 0;
+    const int comb_member = Cfg::kCombGroups > 1 ? warp % Cfg::kCombSize : warp;
 #pragma unroll 1
-    for (int w = 0; w < W; ++w) {
-      if (warp == w) {
+    for (int w = 0; w < Cfg::kCombSize; ++w) {
+      if (comb_member == w) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int r = 8 * nt + 2 * t + c;
-            float4* dst = reinterpret_cast<float4*>(sO + (size_t)r * kHeadDim + 16 * g);
+            float4* dst = reinterpret_cast<float4*>(sO + ((size_t)comb_group * RP + r) * kHeadDim +
+                                                    16 * g);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               float4 v = make_float4(o[2 * k4][nt][c] * fw[nt][c], o[2 * k4][nt][c + 2] * fw[nt][c],
@@ -710,7 +722,9 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
       float l = 0.f;
 #pragma unroll
       for (int w = 0; w < W; ++w) l += ex2(sML[(w * 2) * RP + r] - M) * sML[(w * 2 + 1) * RP + r];
-      const float acc = sO[(size_t)r * kHeadDim + d];
+      float acc = sO[(size_t)r * kHeadDim + d];
+#pragma unroll
+      for (int gi = 1; gi < Cfg::kCombGroups; ++gi) acc += sO[((size_t)gi * RP + r) * kHeadDim + d];
       if (cnt == 1) {
         const int i = r / p.group, gh = r % p.group;
         const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
