@@ -30,12 +30,18 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codec import dequantize, quantize
+from .codec import INT8_TOKEN, dequantize, int8_row_scale, quantize
 
 
 def new_pool(num_pages, num_kv_heads, head_dim, kv_dtype, page_size=16, fill=0):
     dt = np.uint16 if kv_dtype == 0 else np.uint8
     return np.full((num_pages, num_kv_heads, 2, page_size, head_dim), fill, dtype=dt)
+
+
+def new_scale_pool(num_pages, num_kv_heads, page_size=16):
+    """Per-row scales of a format-3 pool: float32 [num_pages, Hkv, page_size]
+    (one for K and one for V), slot t of the pool at [t // P, :, t % P]."""
+    return np.zeros((num_pages, num_kv_heads, page_size), dtype=np.float32)
 
 
 def kv_append_quant(k, v, slot_mapping, kv_dtype, k_scale, v_scale, pages):
@@ -44,7 +50,14 @@ def kv_append_quant(k, v, slot_mapping, kv_dtype, k_scale, v_scale, pages):
     k, v: fp16 [T, Hkv, D]; slot_mapping: int [T] (negative = skip the token);
     k_scale, v_scale: one value, or one per kv-head.  Tokens are written in
     order, so a later token wins if two share a slot.
+
+    Format 3 (INT8 with a scale per row): k_scale and v_scale are the scale
+    pools [num_pages, Hkv, P]; every written row's scale is computed from the
+    row and stored at its slot, and (pages, k_scale, v_scale) copies are
+    returned.
     """
+    if kv_dtype == INT8_TOKEN:
+        return _append_row_scaled(k, v, slot_mapping, k_scale, v_scale, pages)
     k = np.asarray(k, dtype=np.float16)
     v = np.asarray(v, dtype=np.float16)
     out = np.array(pages, copy=True)
@@ -68,14 +81,44 @@ def kv_append_quant(k, v, slot_mapping, kv_dtype, k_scale, v_scale, pages):
     return out
 
 
+def _append_row_scaled(k, v, slot_mapping, k_pool, v_pool, pages):
+    k = np.asarray(k, dtype=np.float16)
+    v = np.asarray(v, dtype=np.float16)
+    out = np.array(pages, copy=True)
+    kp = np.array(k_pool, dtype=np.float32, copy=True)
+    vp = np.array(v_pool, dtype=np.float32, copy=True)
+    P = out.shape[3]
+    slots = np.asarray(slot_mapping, dtype=np.int64).reshape(-1)
+    keep = np.nonzero(slots >= 0)[0]
+    if keep.size == 0:
+        return out, kp, vp
+    if slots[keep].max() >= out.shape[0] * P:
+        raise IndexError("slot %d outside the pool" % slots[keep].max())
+    _, last_rev = np.unique(slots[keep][::-1], return_index=True)
+    keep = np.sort(keep[::-1][last_rev])
+    page, off = np.divmod(slots[keep], P)
+    for h in range(k.shape[1]):
+        ks = int8_row_scale(k[keep, h])
+        vs = int8_row_scale(v[keep, h])
+        out[page, h, 0, off] = quantize(k[keep, h], ks, INT8_TOKEN)
+        out[page, h, 1, off] = quantize(v[keep, h], vs, INT8_TOKEN)
+        kp[page, h, off] = ks
+        vp[page, h, off] = vs
+    return out, kp, vp
+
+
 def gather_kv(pages, block_row, L, h, kv_dtype, k_scale, v_scale):
     """Dequantized float64 K and V [L, D] of one sequence and kv-head, read
-    page by page through its block-table row."""
+    page by page through its block-table row.  For format 3 the scales are the
+    scale pools and each row takes the scale stored at its slot."""
     P = pages.shape[3]
     n = (L + P - 1) // P
     ids = np.asarray(block_row[:n], dtype=np.int64)
     kc = pages[ids, h, 0].reshape(n * P, -1)[:L]
     vc = pages[ids, h, 1].reshape(n * P, -1)[:L]
+    if kv_dtype == INT8_TOKEN:
+        k_scale = np.asarray(k_scale)[ids, h].reshape(-1)[:L]
+        v_scale = np.asarray(v_scale)[ids, h].reshape(-1)[:L]
     return dequantize(kc, k_scale, kv_dtype), dequantize(vc, v_scale, kv_dtype)
 
 
@@ -147,8 +190,11 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
         L = int(seq_lens[s])
         limits = np.repeat(L - q_len + np.arange(q_len), G)
         for h in (range(H) if heads is None else heads):
-            K, V = gather_kv(pages, block_table[s], L, h, kv_dtype,
-                             _scale_of(k_scale, h), _scale_of(v_scale, h))
+            if kv_dtype == INT8_TOKEN:
+                K, V = gather_kv(pages, block_table[s], L, h, kv_dtype, k_scale, v_scale)
+            else:
+                K, V = gather_kv(pages, block_table[s], L, h, kv_dtype,
+                                 _scale_of(k_scale, h), _scale_of(v_scale, h))
             rows = _rows_of(q, s, h, q_len, G)
             bounds = [(L * p) // num_splits for p in range(num_splits + 1)]
             parts = [attention_partial(rows, K, V, limits, bounds[p], bounds[p + 1])

@@ -13,6 +13,12 @@ Formats
   layer's largest value to the largest finite code.
 * INT8 is symmetric: code = clamp(round_half_even(x), -127, 127), value =
   code * scale (ReVolta README, "Weight and KV formats", "INT8 KV").
+* INT8 with a scale per row (format 3): the same codes, but every (token,
+  kv-head) row of K and of V carries its own scale, computed when the row is
+  written -- the README's INT8 KV, whose scales come from the data at run time
+  for each token and head instead of from a calibration.  The scale is the
+  row's largest |x| (NaNs ignored; 0 for a row of zeros) divided by 127,
+  rounded once to binary32; each element is then encoded as above under it.
 
 Rounding is to nearest with ties to even everywhere; encoding saturates.
 For non-finite inputs the oracle takes the reading that E4M3 maps NaN to the
@@ -25,6 +31,7 @@ import numpy as np
 
 E4M3_MAX = 448.0
 INT8_MAX = 127
+INT8_TOKEN = 3          # kv format code: INT8 with a scale per (token, kv-head) row
 
 
 def e4m3_decode(codes) -> np.ndarray:
@@ -96,6 +103,15 @@ def scaled_input(x16, scale) -> np.ndarray:
     return (xf / sf).astype(np.float32).astype(np.float64)
 
 
+def int8_row_scale(x16) -> np.ndarray:
+    """binary32 scale of each row (last axis) of fp16 values for format 3:
+    fp32(amax / 127), amax = the row's largest |x| with NaNs ignored (0 when
+    nothing else is left).  The quotient of two exact values is rounded once."""
+    a = np.abs(np.asarray(x16, dtype=np.float16).astype(np.float64))
+    a = np.where(np.isnan(a), 0.0, a)
+    return (a.max(axis=-1) / INT8_MAX).astype(np.float32)
+
+
 def quantize(x16, scale, kv_dtype: int) -> np.ndarray:
     """Codes stored in the pool for fp16 inputs x16 under ``scale``.
 
@@ -105,10 +121,14 @@ def quantize(x16, scale, kv_dtype: int) -> np.ndarray:
     x16 = np.asarray(x16, dtype=np.float16)
     if kv_dtype == 0:
         return x16.view(np.uint16).copy()
-    v = scaled_input(x16, scale)
+    if kv_dtype == INT8_TOKEN:
+        # ``scale`` holds one value per row (the leading axes of x16)
+        scale = np.asarray(scale, dtype=np.float32)[..., None]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        v = scaled_input(x16, scale)          # a zero scale leaves 0/0 = NaN -> code 0
     if kv_dtype == 1:
         return e4m3_encode(v)
-    if kv_dtype == 2:
+    if kv_dtype in (2, INT8_TOKEN):
         return int8_encode(v).view(np.uint8)
     raise ValueError(kv_dtype)
 
@@ -123,4 +143,6 @@ def dequantize(codes, scale, kv_dtype: int) -> np.ndarray:
         return e4m3_decode(codes.astype(np.uint8)) * s
     if kv_dtype == 2:
         return int8_decode(codes.astype(np.uint8).view(np.int8)) * s
+    if kv_dtype == INT8_TOKEN:
+        return int8_decode(codes.astype(np.uint8).view(np.int8)) * s[..., None]
     raise ValueError(kv_dtype)
