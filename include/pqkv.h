@@ -23,6 +23,11 @@
  * s / page_size.  For one (page, kv-head) the K tile and the V tile are
  * contiguous (4 KB for 8-bit codes), which is what the attention kernel
  * streams.
+ * PQKV_KV_INT8_ROW pools carry a scale area right after the codes, in the same
+ * allocation (num_pages*num_kv_heads*4096 bytes from the start of `pages`):
+ *   float row_scale[num_pages][num_kv_heads][2][page_size]
+ * (index 0 of the third axis: K rows, 1: V rows), i.e. 128 bytes per
+ * (page, kv-head); the allocation is num_pages*num_kv_heads*4224 bytes.
  *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers owned by the caller.  Nothing
@@ -49,7 +54,12 @@ extern "C" {
 typedef enum {
   PQKV_KV_FP16 = 0,     /* fp16 values, scales ignored                          */
   PQKV_KV_FP8_E4M3 = 1, /* OCP E4M3 ("FN": max 448, no Inf), value = dec(c)*scale */
-  PQKV_KV_INT8 = 2      /* symmetric int8 in [-127, 127], value = c*scale         */
+  PQKV_KV_INT8 = 2,     /* symmetric int8 in [-127, 127], value = c*scale         */
+  PQKV_KV_INT8_ROW = 3  /* int8 with its own scale per (token, kv-head) row of K
+                           and of V, computed when the row is written (ReVolta
+                           README, "Weight and KV formats", "INT8 KV": scales
+                           derived from the data at run time, no calibration);
+                           value = c * row_scale.  Scale area: see the layout. */
 } pqkv_kv_dtype;
 
 /* Host-side return codes. */
@@ -94,6 +104,13 @@ enum {
  *           NaN -> 0x7F), zero keeps its sign;
  *     INT8: round half to even, clamp to [-127, 127] (NaN -> 0);
  *     FP16: the fp16 bits unchanged (scales ignored, may be NULL).
+ * INT8_ROW: for each written (token, kv-head) row x of K (and of V) the row's
+ * scale r = fp32(amax / 127), amax = the largest |x_d| of the row (NaNs
+ * ignored; 0 for a row of zeros), correctly rounded, is stored in the scale
+ * area at the row's slot and the codes are the INT8 codes of fp32(x_d) / r
+ * (a zero r gives 0/0 = NaN -> code 0).  k_scale / v_scale are ignored (may
+ * be NULL).  V rows with amax above 32512 exceed what the attention kernel's
+ * fp16 products hold (probability <= 256 times the row scale).
  *
  *   k, v            fp16 [num_tokens][num_kv_heads][head_dim]; heads and dims
  *                   contiguous, tokens `k_token_stride` / `v_token_stride`
@@ -148,7 +165,9 @@ size_t pqkv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len,
  *   block_table       int32 [num_seqs][max_pages_per_seq]: the pool page of
  *                     each logical 16-token page of the sequence.
  *   seq_lens          int32 [num_seqs] (device), q_len <= L <= max_pages_per_seq*16.
- *   k_scale, v_scale  fp32 [1] or [num_kv_heads] (device); ignored for FP16.
+ *   k_scale, v_scale  fp32 [1] or [num_kv_heads] (device); ignored for FP16
+ *                     and INT8_ROW (whose K_j, V_j use the row scales stored
+ *                     at token j's slot).
  *   num_splits        0: balanced split -- the key pages of all sequences and
  *                     kv-heads are cut into one equal contiguous share per
  *                     resident thread block, and a sequence's shares are

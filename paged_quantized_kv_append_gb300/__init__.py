@@ -24,7 +24,9 @@ import torch
 FP16 = 0
 FP8_E4M3 = 1
 INT8 = 2
-KV_DTYPES = {"fp16": FP16, "fp8_e4m3": FP8_E4M3, "int8": INT8}
+INT8_ROW = 3          # int8 with a scale per (token, kv-head) row, computed at append time
+KV_DTYPES = {"fp16": FP16, "fp8_e4m3": FP8_E4M3, "int8": INT8, "int8_row": INT8_ROW}
+_SCALED = (FP8_E4M3, INT8)   # formats that take k_scale / v_scale arguments
 
 HEAD_DIM = 128
 PAGE_SIZE = 16
@@ -103,14 +105,41 @@ def _dtype_id(kv_dtype) -> int:
     return int(kv_dtype)
 
 
+def _row_scale_bytes(num_pages, num_kv_heads):
+    return num_pages * num_kv_heads * 2 * PAGE_SIZE * 4
+
+
 def new_pages(num_pages: int, num_kv_heads: int, kv_dtype, device="cuda", fill=None):
-    """Allocate a pool [num_pages, num_kv_heads, 2, 16, 128] for ``kv_dtype``."""
+    """Allocate a pool [num_pages, num_kv_heads, 2, 16, 128] for ``kv_dtype``.
+
+    An INT8_ROW pool is the code tensor followed, in the same allocation, by
+    its row-scale area (zeroed); ``row_scales(pages)`` views that area.
+    """
     kd = _dtype_id(kv_dtype)
     dt = torch.float16 if kd == FP16 else torch.uint8
     shape = (num_pages, num_kv_heads, 2, PAGE_SIZE, HEAD_DIM)
+    if kd == INT8_ROW:
+        codes = num_pages * num_kv_heads * 2 * PAGE_SIZE * HEAD_DIM
+        buf = torch.zeros(codes + _row_scale_bytes(num_pages, num_kv_heads), dtype=torch.uint8,
+                          device=device)
+        if fill is not None:
+            buf[:codes].fill_(fill)
+        return buf[:codes].view(shape)
     if fill is None:
         return torch.empty(shape, dtype=dt, device=device)
     return torch.full(shape, fill, dtype=dt, device=device)
+
+
+def row_scales(pages: torch.Tensor) -> torch.Tensor:
+    """float32 [num_pages, Hkv, 2, 16] view of an INT8_ROW pool's row scales
+    (index 0 of the third axis: K rows, 1: V rows)."""
+    _check_pages(pages, INT8_ROW)
+    n, H = pages.shape[0], pages.shape[1]
+    codes = pages.numel()
+    whole = torch.empty(0, dtype=torch.uint8, device=pages.device)
+    whole.set_(pages.untyped_storage(), pages.storage_offset(),
+               (codes + _row_scale_bytes(n, H),))
+    return whole[codes:].view(torch.float32).view(n, H, 2, PAGE_SIZE)
 
 
 def _check_pages(pages, kd):
@@ -120,6 +149,11 @@ def _check_pages(pages, kd):
                          % (want, pages.dtype, tuple(pages.shape)))
     if not pages.is_contiguous() or not pages.is_cuda:
         raise ValueError("pages must be a contiguous CUDA tensor")
+    if kd == INT8_ROW:
+        room = pages.untyped_storage().nbytes() - pages.storage_offset()
+        if room < pages.numel() + _row_scale_bytes(pages.shape[0], pages.shape[1]):
+            raise ValueError("an int8_row pool needs its row-scale area after the codes "
+                             "(allocate it with new_pages)")
 
 
 def _check_scale(x, H, name):
@@ -144,14 +178,14 @@ def kv_append_quant(k, v, slot_mapping, kv_dtype, k_scale, v_scale, pages, statu
     if v.shape[0] != T or slot_mapping.dtype != torch.int64 or slot_mapping.shape != (T,):
         raise ValueError("v / slot_mapping do not match k's token count")
     sph = 0
-    if kd != FP16:
+    if kd in _SCALED:
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
     lib = load_library()
     rc = lib.pqkv_kv_append_quant(
         _ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), T, H, HEAD_DIM, kd,
-        _ptr(k_scale if kd != FP16 else None), _ptr(v_scale if kd != FP16 else None), sph,
+        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
         _ptr(pages), pages.shape[0], PAGE_SIZE, _ptr(status), _stream(pages, stream))
     _check(rc, "kv_append_quant")
     return pages
@@ -216,7 +250,7 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
         raise ValueError("q has %d rows, expected num_seqs*q_len = %d" % (q.shape[0], B * q_len))
     Hq = q.shape[1]
     sph = 0
-    if kd != FP16:
+    if kd in _SCALED:
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
@@ -229,7 +263,7 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
     rc = lib.pqkv_paged_attention(
         _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
-        _ptr(k_scale if kd != FP16 else None), _ptr(v_scale if kd != FP16 else None), sph,
+        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
         num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention")
     return out
@@ -261,14 +295,14 @@ def paged_attention_noalloc(q, pages, block_table, seq_lens, q_len, kv_dtype, k_
     if q.shape[0] != B * q_len:
         raise ValueError("q has %d rows, expected num_seqs*q_len = %d" % (q.shape[0], B * q_len))
     sph = 0
-    if kd != FP16:
+    if kd in _SCALED:
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
     rc = load_library().pqkv_paged_attention_noalloc(
         _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), B, q_len, q.shape[1], H, HEAD_DIM, PAGE_SIZE, kd,
-        _ptr(k_scale if kd != FP16 else None), _ptr(v_scale if kd != FP16 else None), sph,
+        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
         num_splits, max_seq_len, _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention_noalloc")
     return out

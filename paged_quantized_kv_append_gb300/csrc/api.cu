@@ -59,11 +59,23 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int elem_bytes(int kv_dtype) { return kv_dtype == PQKV_KV_FP16 ? 2 : 1; }
 
+// formats whose k_scale / v_scale arguments are read
+bool uses_scale_args(int kv_dtype) {
+  return kv_dtype == PQKV_KV_FP8_E4M3 || kv_dtype == PQKV_KV_INT8;
+}
+
+// INT8_ROW: the row scales follow the codes in the pool allocation
+float* row_scale_area(void* pages, int64_t num_pages, int32_t num_kv_heads) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(pages) +
+                                  num_pages * num_kv_heads * 2 * kPageSize * kHeadDim);
+}
+
 int blocks_per_sm(int kv_dtype, int nt, int num_seqs) {
   switch (kv_dtype) {
     case PQKV_KV_FP16: return attention_blocks_per_sm_fp16(nt, num_seqs);
     case PQKV_KV_FP8_E4M3: return attention_blocks_per_sm_e4m3(nt, num_seqs);
     case PQKV_KV_INT8: return attention_blocks_per_sm_int8(nt, num_seqs);
+    case PQKV_KV_INT8_ROW: return attention_blocks_per_sm_int8_row(nt, num_seqs);
   }
   return 0;
 }
@@ -100,7 +112,7 @@ int plan_attention(int32_t num_seqs, int32_t q_len, int32_t hq, int32_t hkv, int
 }
 
 int validate_common(int32_t head_dim, int32_t page_size, int32_t kv_dtype) {
-  if (kv_dtype < PQKV_KV_FP16 || kv_dtype > PQKV_KV_INT8) return PQKV_EINVAL;
+  if (kv_dtype < PQKV_KV_FP16 || kv_dtype > PQKV_KV_INT8_ROW) return PQKV_EINVAL;
   if (head_dim != kHeadDim || page_size != kPageSize) return PQKV_EUNSUPPORTED;
   return PQKV_OK;
 }
@@ -129,7 +141,7 @@ extern "C" int pqkv_kv_append_quant(const void* k, int64_t k_token_stride, const
   if (num_tokens < 0 || num_kv_heads < 1 || num_pages < 0) return PQKV_EINVAL;
   if (num_tokens == 0) return PQKV_OK;
   if (!k || !v || !slot_mapping || !pages) return PQKV_EINVAL;
-  if (kv_dtype != PQKV_KV_FP16 && (!k_scale || !v_scale)) return PQKV_EINVAL;
+  if (uses_scale_args(kv_dtype) && (!k_scale || !v_scale)) return PQKV_EINVAL;
   if (k_token_stride < (int64_t)num_kv_heads * head_dim ||
       v_token_stride < (int64_t)num_kv_heads * head_dim)
     return PQKV_EINVAL;
@@ -152,6 +164,8 @@ extern "C" int pqkv_kv_append_quant(const void* k, int64_t k_token_stride, const
   p.num_kv_heads = num_kv_heads;
   p.pages = static_cast<uint8_t*>(pages);
   p.num_pages = num_pages;
+  p.row_scales = kv_dtype == PQKV_KV_INT8_ROW ? row_scale_area(pages, num_pages, num_kv_heads)
+                                              : nullptr;
   p.status = status;
   const int64_t work = (int64_t)num_tokens * num_kv_heads * (kHeadDim / 16);
   const int64_t blocks = (work + 255) / 256;
@@ -188,7 +202,7 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   if (num_splits < 0 || num_splits > PQKV_MAX_SPLITS) return PQKV_ERANGE;
   if (num_seqs == 0) return PQKV_OK;
   if (!q || !out || !pages || !block_table || !seq_lens) return PQKV_EINVAL;
-  if (kv_dtype != PQKV_KV_FP16 && (!k_scale || !v_scale)) return PQKV_EINVAL;
+  if (uses_scale_args(kv_dtype) && (!k_scale || !v_scale)) return PQKV_EINVAL;
   if (num_pages < 1 || num_pages > INT32_MAX || max_pages_per_seq < 1) return PQKV_EINVAL;
   if ((int64_t)max_pages_per_seq * page_size > PQKV_MAX_SEQ_LEN + page_size) return PQKV_ERANGE;
   if (max_seq_len < 0) return PQKV_EINVAL;
@@ -250,7 +264,10 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   p.out = static_cast<uint16_t*>(out);
   p.block_table = block_table;
   p.seq_lens = seq_lens;
-  p.k_scale = k_scale;
+  // INT8_ROW reads no scale arguments: its k_scale slot carries the row-scale area
+  p.k_scale = kv_dtype == PQKV_KV_INT8_ROW
+                  ? row_scale_area(const_cast<void*>(pages), num_pages, num_kv_heads)
+                  : k_scale;
   p.v_scale = v_scale;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = pl.total ? reinterpret_cast<int32_t*>(ws) : nullptr;
@@ -276,6 +293,7 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   switch (kv_dtype) {
     case PQKV_KV_FP16: e = launch_attention_fp16(p, map, grid, nt, st); break;
     case PQKV_KV_FP8_E4M3: e = launch_attention_e4m3(p, map, grid, nt, st); break;
+    case PQKV_KV_INT8_ROW: e = launch_attention_int8_row(p, map, grid, nt, st); break;
     default: e = launch_attention_int8(p, map, grid, nt, st); break;
   }
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;

@@ -10,6 +10,12 @@
 // store; 32 B for fp16).  Consecutive threads cover consecutive vectors of a
 // row, so loads are fully coalesced and each (token, head) row lands as one
 // 128-byte line of its page tile.
+//
+// INT8 with a scale per row (the README's INT8 KV with run-time scales): the
+// eight threads of a row -- eight consecutive lanes of one warp -- exchange
+// their partial |x| maxima with shuffles, divide the row maximum by 127, encode
+// under that scale and the row's first thread stores the scale at the row's
+// slot of the scale area that follows the codes.
 #include "pqkv_common.cuh"
 
 namespace pqkv {
@@ -29,6 +35,26 @@ __device__ __forceinline__ uint32_t int8_from_f32(float x) {
 }
 
 __device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.4e38f; }
+
+// largest |x| of 16 fp16 values (NaNs drop out of fmaxf), starting from 0
+__device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    m = fmaxf(m, fmaxf(fabsf(__low2float(h)), fabsf(__high2float(h))));
+  }
+  return m;
+}
+
+// maximum over the 8 consecutive lanes that hold one row
+__device__ __forceinline__ float row_max8(float m) {
+  const unsigned mask = 0xFFu << (threadIdx.x & 24);
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, o));
+  return m;
+}
 
 // 16 fp16 values (as 8 words) -> 16 codes (4 words)
 template <int KVT>
@@ -87,6 +113,17 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       reinterpret_cast<uint4*>(kd)[1] = k1;
       reinterpret_cast<uint4*>(vd)[0] = v0;
       reinterpret_cast<uint4*>(vd)[1] = v1;
+    } else if (KVT == PQKV_KV_INT8_ROW) {
+      // all eight threads of the row reach this point together
+      const float kscale = __fdiv_rn(row_max8(amax16(k0, k1)), 127.f);
+      const float vscale = __fdiv_rn(row_max8(amax16(v0, v1)), 127.f);
+      *reinterpret_cast<uint4*>(kd) = quantize16<PQKV_KV_INT8>(k0, k1, kscale);
+      *reinterpret_cast<uint4*>(vd) = quantize16<PQKV_KV_INT8>(v0, v1, vscale);
+      if (c == 0) {
+        float* rs = p.row_scales + (page * p.num_kv_heads + h) * 2 * kPageSize + off;
+        rs[0] = kscale;
+        rs[kPageSize] = vscale;
+      }
     } else {
       const int sh = p.scale_per_head ? h : 0;
       const float kscale = __ldg(p.k_scale + sh);
@@ -111,6 +148,9 @@ cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStr
       break;
     case PQKV_KV_INT8:
       append_kernel<PQKV_KV_INT8><<<grid, 256, 0, stream>>>(p);
+      break;
+    case PQKV_KV_INT8_ROW:
+      append_kernel<PQKV_KV_INT8_ROW><<<grid, 256, 0, stream>>>(p);
       break;
     default:
       return cudaErrorInvalidValue;

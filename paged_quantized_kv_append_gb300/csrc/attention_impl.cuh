@@ -69,7 +69,11 @@ struct AttnCfg {
   static constexpr int kMLOff = kOOff + kCombGroups * kOBytes;
   static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
   static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
-  static constexpr int kBarOff = kQfOff + kQfBytes;
+  // INT8_ROW: the 32 row scales (16 K, 16 V) of each stage's (page, kv-head)
+  static constexpr bool kRowScaled = (KVT == PQKV_KV_INT8_ROW);
+  static constexpr int kScOff = kQfOff + kQfBytes;
+  static constexpr int kScBytes = kRowScaled ? kStages * 128 : 0;
+  static constexpr int kBarOff = kScOff + kScBytes;
   static constexpr int kMiscOff = kBarOff + kStages * 8;
   static constexpr int kMiscBytes = 64 + kW * 4 + 2 * kRP * 4 + 128;
   static constexpr int kPreOff = kMiscOff + kMiscBytes;
@@ -461,8 +465,25 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
     const int h = __shfl_sync(0xffffffffu, cur_h, u - ubase);
     if (lane == 0) {
       const int stage = i % S;
-      mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
-      tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, h, id, policy);
+      if constexpr (Cfg::kRowScaled) {
+        // the page's 32 row scales travel with its tile (one bulk copy on the
+        // same barrier); a page id outside the pool (reported, its codes read
+        // as zeros) gets zero scales, written before the barrier is armed
+        float* dst = reinterpret_cast<float*>(smem + Cfg::kScOff) + stage * 32;
+        const bool id_ok = id >= 0 && (int64_t)id < p.num_pages;
+        if (!id_ok) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) reinterpret_cast<float4*>(dst)[k] = make_float4(0, 0, 0, 0);
+        }
+        mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes + (id_ok ? 128 : 0));
+        tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, h, id, policy);
+        if (id_ok)
+          bulk_load(dst, p.k_scale + ((int64_t)id * p.num_kv_heads + h) * 32, 128,
+                    &full[stage], policy);
+      } else {
+        mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
+        tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, h, id, policy);
+      }
     }
     issued_u = u + 1;
   };
@@ -511,7 +532,8 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         }
       }
       const int sh = p.scale_per_head ? f_h : 0;
-      if (KVT == PQKV_KV_FP16) {
+      if constexpr (KVT == PQKV_KV_FP16 || KVT == PQKV_KV_INT8_ROW) {
+        // FP16 has no scale; INT8_ROW applies its row scales per token
         qk_scale = p.sm_scale_log2;
         v_mult = 1.f;
       } else {
@@ -578,6 +600,18 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
       page_qk<KVT, NT>(T, g, t, lane, qf, sc);
+      if constexpr (Cfg::kRowScaled) {
+        // INT8_ROW: scores of token g and token g+8 times their K row scales
+        const float* rs = reinterpret_cast<const float*>(smem + Cfg::kScOff) + stage * 32;
+        const float ks_g = rs[g], ks_g8 = rs[g + 8];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          sc[nt][0] *= ks_g;
+          sc[nt][1] *= ks_g;
+          sc[nt][2] *= ks_g8;
+          sc[nt][3] *= ks_g8;
+        }
+      }
 
       // Raw scores; masked -> -inf.  The log2-domain score is sc * qk_scale.
       if (pos0 + kPageSize - 1 > lim_min) {
@@ -631,8 +665,19 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         for (int e = 0; e < 4; ++e) pr[e] = ex2(fmaf(sc[nt][e], qk_scale, -mref[nt][e & 1]));
         lsum[nt][0] += pr[0] + pr[2];
         lsum[nt][1] += pr[1] + pr[3];
-        pb[nt][0] = movmatrix_trans(pack_half2(pr[0], pr[1]));
-        pb[nt][1] = movmatrix_trans(pack_half2(pr[2], pr[3]));
+        if constexpr (Cfg::kRowScaled) {
+          // O accumulates p_j * vscale_j * vcode_j; the row sums keep p_j
+          // alone.  Tokens past the sequence end may hold stale scales, and
+          // their probability 0 must not meet a NaN.
+          const float* rs = reinterpret_cast<const float*>(smem + Cfg::kScOff) + stage * 32;
+          const float vs_g = pos0 + g < cur_L ? rs[16 + g] : 0.f;
+          const float vs_g8 = pos0 + g + 8 < cur_L ? rs[24 + g] : 0.f;
+          pb[nt][0] = movmatrix_trans(pack_half2(pr[0] * vs_g, pr[1] * vs_g));
+          pb[nt][1] = movmatrix_trans(pack_half2(pr[2] * vs_g8, pr[3] * vs_g8));
+        } else {
+          pb[nt][0] = movmatrix_trans(pack_half2(pr[0], pr[1]));
+          pb[nt][1] = movmatrix_trans(pack_half2(pr[2], pr[3]));
+        }
       }
       // O^T += V^T P^T
       {

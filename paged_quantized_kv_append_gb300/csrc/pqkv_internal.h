@@ -27,6 +27,7 @@ struct AppendParams {
   int32_t num_kv_heads;
   uint8_t* pages;
   int64_t num_pages;
+  float* row_scales;        // INT8_ROW: [num_pages][Hkv][2][16] after the codes
   int32_t* status;
 };
 
@@ -35,7 +36,7 @@ struct AttnParams {
   uint16_t* out;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  const float* k_scale;
+  const float* k_scale;     // INT8_ROW: the row scales [num_pages][Hkv][2][16]
   const float* v_scale;
   int32_t* counters;        // [B*Hkv] merge tickets (workspace)
   float* part_o;            // [slots][RP][128] unnormalised partial outputs
@@ -61,11 +62,14 @@ cudaError_t launch_attention_e4m3(const AttnParams& p, const CUtensorMap& map, i
                                   int nt, cudaStream_t stream);
 cudaError_t launch_attention_int8(const AttnParams& p, const CUtensorMap& map, int grid,
                                   int nt, cudaStream_t stream);
+cudaError_t launch_attention_int8_row(const AttnParams& p, const CUtensorMap& map, int grid,
+                                      int nt, cudaStream_t stream);
 // Resident blocks per SM of the attention kernel for a KV format, n-tile
 // count and number of sequences (0 if the query fails).
 int attention_blocks_per_sm_fp16(int nt, int num_seqs);
 int attention_blocks_per_sm_e4m3(int nt, int num_seqs);
 int attention_blocks_per_sm_int8(int nt, int num_seqs);
+int attention_blocks_per_sm_int8_row(int nt, int num_seqs);
 
 cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream);
 

@@ -48,12 +48,21 @@ class Case:
     def build_oracle(self, fill=0):
         w = self.w
         pool = oracle.new_pool(self.plan.num_pages, w.num_kv_heads, w.head_dim, w.kv_dtype, fill=fill)
-        ks, vs = self.ks.cpu().numpy(), self.vs.cpu().numpy()
+        if w.kv_dtype == W.INT8_ROW:
+            ks = oracle.new_scale_pool(self.plan.num_pages, w.num_kv_heads)
+            vs = oracle.new_scale_pool(self.plan.num_pages, w.num_kv_heads)
+        else:
+            ks, vs = self.ks.cpu().numpy(), self.vs.cpu().numpy()
         for s, L in enumerate(w.seq_lens):
             k, v = W.kv_tokens(w, s, 0, L, "cpu")
-            pool = oracle.kv_append_quant(k.numpy(), v.numpy(), W.slots_for(self.plan, s, 0, L),
-                                          w.kv_dtype, ks, vs, pool)
+            r = oracle.kv_append_quant(k.numpy(), v.numpy(), W.slots_for(self.plan, s, 0, L),
+                                       w.kv_dtype, ks, vs, pool)
+            if w.kv_dtype == W.INT8_ROW:
+                pool, ks, vs = r
+            else:
+                pool = r
         self.pool_o = pool
+        self.oracle_ks, self.oracle_vs = ks, vs
 
     def gpu_pool_bytes(self):
         x = self.pages.cpu()
@@ -70,8 +79,8 @@ class Case:
     def oracle_attention(self, seqs=None, heads=None):
         w = self.w
         return oracle.paged_attention(self.q.cpu().numpy(), self.pool_o, self.plan.block_table,
-                                      w.seq_lens, w.q_len, w.kv_dtype, self.ks.cpu().numpy(),
-                                      self.vs.cpu().numpy(), seqs=seqs, heads=heads)
+                                      w.seq_lens, w.q_len, w.kv_dtype, self.oracle_ks,
+                                      self.oracle_vs, seqs=seqs, heads=heads)
 
 
 def assert_close(gpu, ref, what=""):

@@ -33,6 +33,14 @@ def test_header_declares_the_entry_points():
             "pqkv_status_string", "pqkv_version"} <= set(names)
 
 
+def test_header_and_binding_agree_on_formats():
+    text = open(HEADER).read()
+    for name, code in (("PQKV_KV_FP16", 0), ("PQKV_KV_FP8_E4M3", 1), ("PQKV_KV_INT8", 2),
+                       ("PQKV_KV_INT8_ROW", 3)):
+        assert re.search(r"\b%s = %d\b" % (name, code), text), name
+    assert (pq.FP16, pq.FP8_E4M3, pq.INT8, pq.INT8_ROW) == (0, 1, 2, 3)
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
@@ -57,7 +65,8 @@ def _append(lib, **kw):
 def test_append_validation(lib):
     assert _append(lib, D=64) == EUNSUPPORTED
     assert _append(lib, P=32) == EUNSUPPORTED
-    assert _append(lib, dt=3) == EINVAL
+    assert _append(lib, dt=4) == EINVAL
+    assert _append(lib, dt=3, kscale=None, vscale=None) == ECUDA   # INT8_ROW needs no scales
     assert _append(lib, T=0) == OK                        # no-op, no CUDA call
     assert _append(lib, k=None) == EINVAL
     assert _append(lib, kscale=None) == EINVAL
@@ -89,6 +98,9 @@ def test_attention_validation(lib):
     assert _attn(lib, B=3000) == ERANGE
     assert _attn(lib, ns=129) == ERANGE
     assert _attn(lib, q=None) == EINVAL
+    assert _attn(lib, dt=4) == EINVAL
+    assert _attn(lib, dt=3, kscale=None, vscale=None) == ECUDA      # INT8_ROW needs no scales
+    assert _attn(lib, dt=2, kscale=None) == EINVAL
     assert _attn(lib, npages=0) == EINVAL
     assert _attn(lib, mpps=40000) == ERANGE               # beyond 524288 tokens
     assert _attn(lib, out=(1 << 12) + 8) == EINVAL        # misaligned

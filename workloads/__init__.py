@@ -48,6 +48,7 @@ HEAD_DIM = 128
 FP16 = 0
 FP8_E4M3 = 1
 INT8 = 2
+INT8_ROW = 3          # INT8 with a scale per (token, kv-head) row, computed at append time
 DTYPE_NAMES = {FP16: "fp16", FP8_E4M3: "fp8_e4m3", INT8: "int8"}
 
 _TABLE_CACHE = {}
@@ -201,6 +202,10 @@ def workload(name: str, scale: float = 1.0) -> Workload:
     if name == "int8_decode_append_262k":
         return Workload(name, 4, [L(262144)] * 4, 32, 8, 1, INT8, scale_per_head=True,
                         pool_slack=0.01, append_per_step=1)
+    if name == "int8_row_decode_262k":       # config 4's shapes with run-time row scales
+        return Workload(name, 6, [L(262144)] * 4, 32, 8, 1, INT8_ROW, pool_slack=0.01)
+    if name == "int8_row_verify_131k":       # config 3's shapes with run-time row scales
+        return Workload(name, 7, [L(131072)] * 8, 32, 8, 5, INT8_ROW, pool_slack=0.01)
     if name == "e4m3_verify_512k_stress":
         return Workload(name, 5, [L(524288)] * 2 + [L(32768)] * 6, 32, 8, 5, FP8_E4M3,
                         pool_slack=0.02, append_tokens=8192 if scale >= 1.0 else 520,
@@ -210,6 +215,8 @@ def workload(name: str, scale: float = 1.0) -> Workload:
 
 WORKLOAD_NAMES = ["tiny_fp16_decode", "e4m3_decode_b8", "e4m3_verify_131k",
                   "int8_decode_append_262k", "e4m3_verify_512k_stress"]
+# INT8 with run-time row scales (the pages' own INT8 design) on configs 4 and 3's shapes
+ROW_SCALED_NAMES = ["int8_row_decode_262k", "int8_row_verify_131k"]
 
 
 @dataclasses.dataclass
@@ -286,11 +293,12 @@ def calibrated_scales(w: Workload, device="cpu"):
     """Per-layer (or per-kv-head for INT8) scales: amax of the layer's fp16 K
     (resp. V) over every cached token, divided by the format's largest value.
 
-    Returns float32 tensors of shape [1] or [Hkv] on ``device``.  FP16 pools
-    take no scale; ones are returned so callers can pass something.
+    Returns float32 tensors of shape [1] or [Hkv] on ``device``.  FP16 and
+    INT8_ROW pools take no scale argument; ones are returned so callers can
+    pass something.
     """
     H = w.num_kv_heads
-    if w.kv_dtype == FP16:
+    if w.kv_dtype in (FP16, INT8_ROW):
         one = torch.ones(H if w.scale_per_head else 1, dtype=torch.float32, device=device)
         return one, one.clone()
     qmax = 448.0 if w.kv_dtype == FP8_E4M3 else 127.0
