@@ -9,11 +9,12 @@ library and never imports it.
 from .codec import (E4M3_MAX, INT8_MAX, INT8_TOKEN, dequantize, e4m3_decode, e4m3_encode,
                     int8_decode, int8_encode, int8_row_scale, quantize, scaled_input)
 from .attention import (attention_partial, dense_attention, gather_kv,
-                        kv_append_quant, lse_merge, new_pool, new_scale_pool, paged_attention)
+                        kv_append_quant, lse_merge, merge_lse, new_pool, new_scale_pool,
+                        paged_attention, paged_attention_partial)
 
 __all__ = [
     "E4M3_MAX", "INT8_MAX", "INT8_TOKEN", "dequantize", "e4m3_decode", "e4m3_encode",
     "int8_decode", "int8_encode", "int8_row_scale", "quantize", "scaled_input",
     "attention_partial", "dense_attention", "gather_kv", "kv_append_quant", "lse_merge",
-    "new_pool", "new_scale_pool", "paged_attention",
+    "merge_lse", "new_pool", "new_scale_pool", "paged_attention", "paged_attention_partial",
 ]

@@ -204,6 +204,54 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
     return out
 
 
+def paged_attention_partial(q, pages, block_table, seq_lens, q_pos, q_len, kv_dtype, k_scale,
+                            v_scale):
+    """One rank's share of a decode context parallel split: attention over the
+    keys held locally (seq_lens[s] of them), query i of sequence s seeing local
+    keys j <= q_pos[s] + i.  Returns float64 (O / l [B * q_len, Hq, D],
+    lse [B * q_len, Hq]) with lse = m + ln l in natural-log units; a row that
+    sees no key gets O = 0 and lse = -inf."""
+    q = np.asarray(q)
+    BQ, Hq, D = q.shape
+    H = pages.shape[1]
+    G = Hq // H
+    o = np.zeros((BQ, Hq, D))
+    lse = np.full((BQ, Hq), -np.inf)
+    for s in range(len(seq_lens)):
+        L = int(seq_lens[s])
+        limits = np.repeat(int(q_pos[s]) + np.arange(q_len), G)
+        for h in range(H):
+            if L == 0:
+                continue
+            if kv_dtype == INT8_TOKEN:
+                K, V = gather_kv(pages, block_table[s], L, h, kv_dtype, k_scale, v_scale)
+            else:
+                K, V = gather_kv(pages, block_table[s], L, h, kv_dtype,
+                                 _scale_of(k_scale, h), _scale_of(v_scale, h))
+            O, m, l = attention_partial(_rows_of(q, s, h, q_len, G), K, V, limits, 0, L)
+            seen = l > 0
+            O[seen] /= l[seen][:, None]
+            lr = np.where(seen, m + np.log(np.where(seen, l, 1.0)), -np.inf)
+            o[s * q_len:(s + 1) * q_len, h * G:(h + 1) * G] = O.reshape(q_len, G, D)
+            lse[s * q_len:(s + 1) * q_len, h * G:(h + 1) * G] = lr.reshape(q_len, G)
+    return o, lse
+
+
+def merge_lse(parts_o, parts_lse):
+    """Combine partial results in (O / l, lse) form over the leading axis:
+    LSE = ln sum_p e^{lse_p}, O = sum_p e^{lse_p - LSE} O_p.  Rows with no
+    finite lse_p give O = 0, LSE = -inf."""
+    po = np.asarray(parts_o, dtype=np.float64)
+    pl = np.asarray(parts_lse, dtype=np.float64)
+    M = pl.max(axis=0)
+    finite = np.isfinite(M)
+    w = np.where(finite[None], np.exp(pl - np.where(finite, M, 0.0)[None]), 0.0)
+    tot = w.sum(axis=0)
+    o = np.einsum("p...,p...d->...d", w, po) / np.where(tot > 0, tot, 1.0)[..., None]
+    lse = np.where(tot > 0, np.where(finite, M, 0.0) + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    return o, lse
+
+
 def dense_attention(q_rows, K, V, limits):
     """Attention of query rows over dense float64 K, V [L, D] (no pages)."""
     O, m, l = attention_partial(np.asarray(q_rows, np.float64), K, V, limits, 0, K.shape[0])

@@ -71,3 +71,48 @@ def test_clock_sampler_keeps_only_the_timed_window(tmp_path):
     r = bench.ClockSampler.summarize(str(p), t0, t1)
     assert r["sm_mhz"] == 1925.0 and r["sm_max_mhz"] == 2070.0
     assert r["reasons"] == [] and r["samples_in_timed_region"] == 2 and r["samples_total"] == 3
+
+
+def _dcp_rank(rank, world, port, out):
+    """One CPU rank of a decode context parallel split: the oracle attends over
+    this rank's page-aligned share of every sequence's keys, the ranks
+    all-gather (O / l, lse) over gloo, and every rank merges."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import oracle
+    from tests.test_oracle_attention import _random_case
+    from tests.test_oracle_dcp import shares
+    dist.init_process_group("gloo")
+    rng = np.random.default_rng(31)                      # same data on every rank
+    q, pool, bt, L, ks, vs = _random_case(rng, [45, 70, 9], 2, 4, 16, 5, 1)
+    bounds = [(0, 2), (2, 8)][rank:rank + 1]
+    (lbt, ls, qp), = shares(bt, L, 5, bounds)
+    o, lse = oracle.paged_attention_partial(q, pool, lbt, ls, qp, 5, 1, ks, vs)
+    go = [torch.zeros(o.shape, dtype=torch.float64) for _ in range(world)]
+    gl = [torch.zeros(lse.shape, dtype=torch.float64) for _ in range(world)]
+    dist.all_gather(go, torch.from_numpy(o))
+    dist.all_gather(gl, torch.from_numpy(lse))
+    merged, _ = oracle.merge_lse([x.numpy() for x in go], [x.numpy() for x in gl])
+    full = oracle.paged_attention(q, pool, bt, L, 5, 1, ks, vs)
+    out[rank] = float(np.abs(merged - full).max())
+    dist.destroy_process_group()
+
+
+def test_dcp_split_over_two_gloo_ranks_equals_full_attention():
+    world = 2
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_dcp_rank, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(180)
+        assert p.exitcode == 0
+    assert set(out.keys()) == {0, 1} and max(out.values()) < 1e-12
