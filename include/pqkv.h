@@ -193,6 +193,53 @@ int pqkv_paged_attention(const void* q, void* out, const void* pages, int64_t nu
                          int32_t max_seq_len, void* workspace, size_t workspace_bytes,
                          int32_t* status, void* stream);
 
+/*
+ * pqkv_paged_attention_partial -- one rank's part of a decode context
+ * parallel split (ReVolta README, "Hardware": TP4 + DCP2; "Quick start",
+ * launch: --decode-context-parallel-size 2): each rank holds a contiguous,
+ * page-aligned share of every sequence's keys, attends over it, and the ranks'
+ * results are combined by pqkv_lse_merge (after an all-gather across ranks).
+ *
+ * Same arguments as pqkv_paged_attention, except:
+ *   seq_lens   int32 [num_seqs]: keys of each sequence held here (0 allowed);
+ *   q_pos      int32 [num_seqs] (device): local index of query 0's position,
+ *              i.e. its global position minus the global index of this
+ *              share's first key; query i sees local keys j <= q_pos + i
+ *              (any value: negative hides every key from the row);
+ *   out_o      fp32 [num_seqs*q_len][num_q_heads][head_dim]: O / l of the
+ *              share (0 for a row that sees no key);
+ *   out_lse    fp32 [num_seqs*q_len][num_q_heads]: m + ln(l), the natural-log
+ *              log-sum-exp of the row's scores over the share (-inf when the
+ *              row sees no key).
+ * Scores are q . K_j / sqrt(head_dim) as in pqkv_paged_attention.  out_o must
+ * be 16-byte aligned.
+ */
+int pqkv_paged_attention_partial(const void* q, const void* pages, int64_t num_pages,
+                                 const int32_t* block_table, int32_t max_pages_per_seq,
+                                 const int32_t* seq_lens, const int32_t* q_pos, int32_t num_seqs,
+                                 int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t page_size, int32_t kv_dtype,
+                                 const float* k_scale, const float* v_scale,
+                                 int32_t scale_per_head, int32_t num_splits, int32_t max_seq_len,
+                                 float* out_o, float* out_lse, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * pqkv_lse_merge -- combine partial results of the same rows (the merge step
+ * of the split above): with parts p = 0 .. num_parts-1,
+ *     LSE = ln sum_p e^{lse_p},   out = sum_p e^{lse_p - LSE} o_p   (fp16)
+ * Parts with lse_p = -inf contribute nothing; a row with no finite lse_p
+ * gets out = 0 and LSE = -inf.
+ *   part_o    fp32 [num_parts][num_rows][head_dim], 16-byte aligned;
+ *   part_lse  fp32 [num_parts][num_rows];
+ *   out       fp16 [num_rows][head_dim], 16-byte aligned;
+ *   out_lse   fp32 [num_rows] or NULL (for a further merge level).
+ * num_rows = num_seqs*q_len*num_q_heads for pqkv_paged_attention_partial's
+ * outputs.  Requires head_dim == 128.
+ */
+int pqkv_lse_merge(const float* part_o, const float* part_lse, int32_t num_parts,
+                   int64_t num_rows, int32_t head_dim, void* out, float* out_lse, void* stream);
+
 /* Size of the library-owned scratch area used by pqkv_paged_attention_noalloc
  * (16 MiB, held on every GPU that loads the library until the process exits). */
 #define PQKV_NOALLOC_SCRATCH_BYTES (16u << 20)

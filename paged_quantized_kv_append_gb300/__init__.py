@@ -73,6 +73,13 @@ def load_library(path: str | None = None):
                                                      c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                                                      c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp,
                                                      c_vp]
+        lib.pqkv_paged_attention_partial.restype = ctypes.c_int
+        lib.pqkv_paged_attention_partial.argtypes = [c_vp, c_vp, c_i64, c_vp, c_i32, c_vp, c_vp,
+                                                     c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                                     c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp,
+                                                     c_vp, c_vp, c_sz, c_vp, c_vp]
+        lib.pqkv_lse_merge.restype = ctypes.c_int
+        lib.pqkv_lse_merge.argtypes = [c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_vp]
         lib.pqkv_status_string.restype = ctypes.c_char_p
         lib.pqkv_status_string.argtypes = [ctypes.c_int]
         lib.pqkv_version.restype = ctypes.c_char_p
@@ -266,6 +273,73 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
         _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
         num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention")
+    return out
+
+
+def paged_attention_partial(q, pages, block_table, seq_lens, q_pos, q_len, kv_dtype, k_scale,
+                            v_scale, out_o, out_lse, num_splits=0, max_seq_len=0, workspace=None,
+                            status=None, stream=None):
+    """One rank's share of a decode-context-parallel split: attention over the
+    keys held here (``seq_lens`` of them per sequence, possibly 0), query i of
+    sequence s seeing local keys j <= q_pos[s] + i.  Writes O / l into
+    ``out_o`` (fp32, shaped like q) and the natural-log LSE into ``out_lse``
+    (fp32 [num_seqs * q_len, Hq]); merge the ranks' results with lse_merge."""
+    kd = _dtype_id(kv_dtype)
+    _check_pages(pages, kd)
+    H = pages.shape[1]
+    if q.dtype != torch.float16 or q.dim() != 3 or q.shape[2] != HEAD_DIM or not q.is_contiguous():
+        raise ValueError("q must be contiguous fp16 [num_seqs*q_len, Hq, 128]")
+    if out_o.shape != q.shape or out_o.dtype != torch.float32 or not out_o.is_contiguous():
+        raise ValueError("out_o must be contiguous fp32 shaped like q")
+    if out_lse.shape != q.shape[:2] or out_lse.dtype != torch.float32 or not out_lse.is_contiguous():
+        raise ValueError("out_lse must be contiguous fp32 [num_seqs*q_len, Hq]")
+    B = seq_lens.shape[0]
+    for name, x in (("seq_lens", seq_lens), ("q_pos", q_pos)):
+        if x.dtype != torch.int32 or x.shape != (B,):
+            raise ValueError("%s must be int32 [num_seqs]" % name)
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous int32 [num_seqs, max_pages_per_seq]")
+    if q.shape[0] != B * q_len:
+        raise ValueError("q has %d rows, expected num_seqs*q_len = %d" % (q.shape[0], B * q_len))
+    Hq = q.shape[1]
+    sph = 0
+    if kd in _SCALED:
+        sph = _check_scale(k_scale, H, "k_scale")
+        if _check_scale(v_scale, H, "v_scale") != sph:
+            raise ValueError("k_scale and v_scale must have the same shape")
+    need = workspace_size(B, q_len, Hq, H, num_splits)
+    if workspace is None:
+        workspace = _default_workspace(q.device)
+    ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load_library().pqkv_paged_attention_partial(
+        _ptr(q), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), _ptr(q_pos), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
+        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
+        num_splits, max_seq_len, _ptr(out_o), _ptr(out_lse), _ptr(ws), ws_bytes, _ptr(status),
+        _stream(q, stream))
+    _check(rc, "paged_attention_partial")
+    return out_o, out_lse
+
+
+def lse_merge(parts_o, parts_lse, out, out_lse=None, stream=None):
+    """Combine partial results: parts_o fp32 [P, rows..., 128], parts_lse fp32
+    [P, rows...] -> out fp16 [rows..., 128] (and the merged LSE if given)."""
+    P = parts_o.shape[0]
+    rows = parts_lse[0].numel()
+    if parts_o.dtype != torch.float32 or not parts_o.is_contiguous() or \
+            parts_o.numel() != P * rows * HEAD_DIM:
+        raise ValueError("parts_o must be contiguous fp32 [P, rows..., 128]")
+    if parts_lse.dtype != torch.float32 or not parts_lse.is_contiguous() or parts_lse.shape[0] != P:
+        raise ValueError("parts_lse must be contiguous fp32 [P, rows...]")
+    if out.dtype != torch.float16 or not out.is_contiguous() or out.numel() != rows * HEAD_DIM:
+        raise ValueError("out must be contiguous fp16 with rows * 128 elements")
+    if out_lse is not None and (out_lse.dtype != torch.float32 or out_lse.numel() != rows):
+        raise ValueError("out_lse must be fp32 with one value per row")
+    rc = load_library().pqkv_lse_merge(_ptr(parts_o), _ptr(parts_lse), P, rows, HEAD_DIM,
+                                       _ptr(out), _ptr(out_lse), _stream(out, stream))
+    _check(rc, "lse_merge")
     return out
 
 

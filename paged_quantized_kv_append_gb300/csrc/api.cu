@@ -186,30 +186,32 @@ extern "C" size_t pqkv_paged_attention_workspace_size(int32_t num_seqs, int32_t 
   return pl.total;
 }
 
-extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
-                                    int64_t num_pages, const int32_t* block_table,
-                                    int32_t max_pages_per_seq, const int32_t* seq_lens,
-                                    int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
-                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
-                                    int32_t kv_dtype, const float* k_scale, const float* v_scale,
-                                    int32_t scale_per_head, int32_t num_splits,
-                                    int32_t max_seq_len, void* workspace, size_t workspace_bytes,
-                                    int32_t* status, void* stream) {
+namespace pqkv {
+namespace {
+
+// Validation, grid, workspace plan and TMA map shared by the attention entry
+// points; fills everything in *p except the output pointer.
+int prepare_attention(const void* q, const void* pages, int64_t num_pages,
+                      const int32_t* block_table, int32_t max_pages_per_seq,
+                      const int32_t* seq_lens, int32_t num_seqs, int32_t q_len,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t page_size, int32_t kv_dtype, const float* k_scale,
+                      const float* v_scale, int32_t scale_per_head, int32_t num_splits,
+                      int32_t max_seq_len, void* workspace, size_t workspace_bytes,
+                      int32_t* status, AttnParams* pp, CUtensorMap* mapp, int* gridp, int* ntp) {
   int rc = validate_common(head_dim, page_size, kv_dtype);
   if (rc) return rc;
   rc = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
   if (rc) return rc;
   if (num_splits < 0 || num_splits > PQKV_MAX_SPLITS) return PQKV_ERANGE;
   if (num_seqs == 0) return PQKV_OK;
-  if (!q || !out || !pages || !block_table || !seq_lens) return PQKV_EINVAL;
+  if (!q || !pages || !block_table || !seq_lens) return PQKV_EINVAL;
   if (uses_scale_args(kv_dtype) && (!k_scale || !v_scale)) return PQKV_EINVAL;
   if (num_pages < 1 || num_pages > INT32_MAX || max_pages_per_seq < 1) return PQKV_EINVAL;
   if ((int64_t)max_pages_per_seq * page_size > PQKV_MAX_SEQ_LEN + page_size) return PQKV_ERANGE;
   if (max_seq_len < 0) return PQKV_EINVAL;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(pages, 16) || !aligned(block_table, 4) ||
-      !aligned(seq_lens, 4))
+  if (!aligned(q, 16) || !aligned(pages, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
     return PQKV_EINVAL;
-
   int sms = 0;
   rc = current_device_sms(&sms);
   if (rc) return rc;
@@ -245,7 +247,7 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   if (!enc) return PQKV_ECUDA;
   const int eb = elem_bytes(kv_dtype);
   const cuuint32_t lines = (cuuint32_t)(2 * page_size * head_dim * eb / 128);
-  CUtensorMap map;
+  CUtensorMap& map = *mapp;
   std::memset(&map, 0, sizeof(map));
   const cuuint64_t dims[4] = {(cuuint64_t)(128 / eb), lines, (cuuint64_t)num_kv_heads,
                               (cuuint64_t)num_pages};
@@ -259,9 +261,9 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return PQKV_ECUDA;
 
-  AttnParams p;
+  AttnParams& p = *pp;
   p.q = static_cast<const uint16_t*>(q);
-  p.out = static_cast<uint16_t*>(out);
+  p.out = nullptr;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   // INT8_ROW reads no scale arguments: its k_scale slot carries the row-scale area
@@ -288,6 +290,38 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   p.num_splits = num_splits;
   p.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
 
+  *gridp = grid;
+  *ntp = nt;
+  return PQKV_OK;
+}
+
+}  // namespace
+}  // namespace pqkv
+
+extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
+                                    int64_t num_pages, const int32_t* block_table,
+                                    int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                    int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                    int32_t kv_dtype, const float* k_scale, const float* v_scale,
+                                    int32_t scale_per_head, int32_t num_splits,
+                                    int32_t max_seq_len, void* workspace, size_t workspace_bytes,
+                                    int32_t* status, void* stream) {
+  if (num_seqs > 0 && (!out || !aligned(out, 16))) {
+    const int rc0 = validate_common(head_dim, page_size, kv_dtype);
+    if (rc0) return rc0;
+    const int rc1 = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
+    return rc1 ? rc1 : PQKV_EINVAL;
+  }
+  AttnParams p;
+  CUtensorMap map;
+  int grid = 0, nt = 0;
+  int rc = prepare_attention(q, pages, num_pages, block_table, max_pages_per_seq, seq_lens,
+                             num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
+                             kv_dtype, k_scale, v_scale, scale_per_head, num_splits, max_seq_len,
+                             workspace, workspace_bytes, status, &p, &map, &grid, &nt);
+  if (rc || num_seqs == 0) return rc;
+  p.out = static_cast<uint16_t*>(out);
   cudaError_t e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (kv_dtype) {
@@ -296,6 +330,58 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
     case PQKV_KV_INT8_ROW: e = launch_attention_int8_row(p, map, grid, nt, st); break;
     default: e = launch_attention_int8(p, map, grid, nt, st); break;
   }
+  return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
+}
+
+extern "C" int pqkv_paged_attention_partial(
+    const void* q, const void* pages, int64_t num_pages, const int32_t* block_table,
+    int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* q_pos, int32_t num_seqs,
+    int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+    int32_t kv_dtype, const float* k_scale, const float* v_scale, int32_t scale_per_head,
+    int32_t num_splits, int32_t max_seq_len, float* out_o, float* out_lse, void* workspace,
+    size_t workspace_bytes, int32_t* status, void* stream) {
+  if (num_seqs > 0 && (!q_pos || !out_o || !out_lse || !aligned(q_pos, 4) ||
+                       !aligned(out_o, 16) || !aligned(out_lse, 4))) {
+    const int rc0 = validate_common(head_dim, page_size, kv_dtype);
+    if (rc0) return rc0;
+    const int rc1 = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
+    return rc1 ? rc1 : PQKV_EINVAL;
+  }
+  AttnPartialParams p;
+  CUtensorMap map;
+  int grid = 0, nt = 0;
+  int rc = prepare_attention(q, pages, num_pages, block_table, max_pages_per_seq, seq_lens,
+                             num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
+                             kv_dtype, k_scale, v_scale, scale_per_head, num_splits, max_seq_len,
+                             workspace, workspace_bytes, status, &p, &map, &grid, &nt);
+  if (rc || num_seqs == 0) return rc;
+  p.q_pos = q_pos;
+  p.out_o = out_o;
+  p.out_lse = out_lse;
+  cudaError_t e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (kv_dtype) {
+    case PQKV_KV_FP16: e = launch_attention_partial_fp16(p, map, grid, nt, st); break;
+    case PQKV_KV_FP8_E4M3: e = launch_attention_partial_e4m3(p, map, grid, nt, st); break;
+    case PQKV_KV_INT8_ROW: e = launch_attention_partial_int8_row(p, map, grid, nt, st); break;
+    default: e = launch_attention_partial_int8(p, map, grid, nt, st); break;
+  }
+  return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
+}
+
+extern "C" int pqkv_lse_merge(const float* part_o, const float* part_lse, int32_t num_parts,
+                              int64_t num_rows, int32_t head_dim, void* out, float* out_lse,
+                              void* stream) {
+  if (head_dim != kHeadDim) return PQKV_EUNSUPPORTED;
+  if (num_parts < 1 || num_rows < 0) return PQKV_EINVAL;
+  if (num_rows == 0) return PQKV_OK;
+  if (num_rows > ((int64_t)1 << 34)) return PQKV_ERANGE;
+  if (!part_o || !part_lse || !out || !aligned(part_o, 16) || !aligned(part_lse, 4) ||
+      !aligned(out, 16) || (out_lse && !aligned(out_lse, 4)))
+    return PQKV_EINVAL;
+  const cudaError_t e = launch_lse_merge(part_o, part_lse, num_parts, num_rows,
+                                         static_cast<uint16_t*>(out), out_lse,
+                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }
 

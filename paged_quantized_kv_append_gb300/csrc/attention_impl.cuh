@@ -88,6 +88,7 @@ struct AttnCfg {
 // Initial reference maximum of a row: finite, so exp2(score - ref) needs no
 // special case, and far below any score (the first page always raises it).
 constexpr float kNoScore = -1.0e30f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -335,10 +336,14 @@ __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int KVT, int NT>
+template <class PP> struct IsPartial { static constexpr bool value = false; };
+template <> struct IsPartial<AttnPartialParams> { static constexpr bool value = true; };
+
+template <int KVT, int NT, class PP = AttnParams>
 __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
-    paged_attention_kernel(const __grid_constant__ CUtensorMap map, const AttnParams p) {
+    paged_attention_kernel(const __grid_constant__ CUtensorMap map, const PP p) {
   using Cfg = AttnCfg<KVT, NT>;
+  constexpr bool kPartial = IsPartial<PP>::value;
   constexpr int W = Cfg::kW, S = Cfg::kStages, SPW = Cfg::kStagesPerWarp, RP = Cfg::kRP;
   constexpr int nthr = W * 32;
   extern __shared__ uint8_t smem_raw[];
@@ -370,9 +375,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   for (int s = tid; s < B; s += nthr) {
     int L = p.seq_lens[s];
     const int Lmax = p.bt_stride * kPageSize;
-    if (L < p.q_len || L > Lmax) {
+    const int Lmin = kPartial ? 0 : p.q_len;    // a rank's share of keys may be empty
+    if (L < Lmin || L > Lmax) {
       if (blockIdx.x == 0) report(p.status, PQKV_DEV_SEQ_RANGE);
-      L = max(p.q_len, min(L, Lmax));
+      L = max(Lmin, min(L, Lmax));
     }
     slen[s] = L;
     pre[s + 1] = (L + kPageSize - 1) / kPageSize;
@@ -398,6 +404,17 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
     }
   }
   __syncthreads();
+
+  if constexpr (kPartial) {
+    // rows of sequences with no local keys: O = 0, LSE = -inf
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+      if (slen[s] != 0) continue;
+      const int64_t r0 = (int64_t)s * p.q_len * p.num_q_heads;
+      const int nr = p.q_len * p.num_q_heads;
+      for (int idx = tid; idx < nr * kHeadDim; idx += nthr) p.out_o[r0 * kHeadDim + idx] = 0.f;
+      for (int idx = tid; idx < nr; idx += nthr) p.out_lse[r0 + idx] = -INFINITY;
+    }
+  }
 
   Split sp;
   sp.pre = pre;
@@ -544,7 +561,8 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         v_mult = vs;
       }
       inv_qk_scale = 1.f / qk_scale;
-      lim_min = L - p.q_len;
+      if constexpr (kPartial) lim_min = p.q_pos[f_s];
+      else lim_min = L - p.q_len;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -774,7 +792,12 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         const int i = r / p.group, gh = r % p.group;
         const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
         const float val = l > 0.f ? acc / l * v_mult : 0.f;
-        p.out[orow * kHeadDim + d] = __half_as_ushort(__float2half_rn(val));
+        if constexpr (kPartial) {
+          p.out_o[orow * kHeadDim + d] = val;
+          if (d == 0) p.out_lse[orow] = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
+        } else {
+          p.out[orow * kHeadDim + d] = __half_as_ushort(__float2half_rn(val));
+        }
       } else {
         p.part_o[((size_t)slot * RP + r) * kHeadDim + d] = acc;
         if (d == 0) {
@@ -845,12 +868,19 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
           const float inv = sLrow[r] > 0.f ? v_mult / sLrow[r] : 0.f;
           const int i = r / p.group, gh = r % p.group;
           const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
-          __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
-          __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&h01);
-          pk.y = *reinterpret_cast<uint32_t*>(&h23);
-          *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+          if constexpr (kPartial) {
+            *reinterpret_cast<float4*>(p.out_o + orow * kHeadDim + 4 * dq) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (dq == 0)
+              p.out_lse[orow] = sLrow[r] > 0.f ? (M + __log2f(sLrow[r])) * kLn2 : -INFINITY;
+          } else {
+            __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
+            __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+          }
         }
         if (tid == 0) p.counters[f_seg] = 0;
       }
@@ -905,6 +935,34 @@ int blocks_per_sm_t(int num_seqs) {
                                                     Cfg::smem_bytes(num_seqs)) != cudaSuccess)
     return 0;
   return n;
+}
+
+template <int KVT, int NT>
+cudaError_t launch_attention_partial_t(const AttnPartialParams& p, const CUtensorMap& map,
+                                       int grid, cudaStream_t stream) {
+  using Cfg = AttnCfg<KVT, NT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<KVT, NT, AttnPartialParams>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::smem_bytes(PQKV_MAX_SEQS));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  paged_attention_kernel<KVT, NT, AttnPartialParams>
+      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
+  return cudaGetLastError();
+}
+
+template <int KVT>
+cudaError_t launch_attention_partial_dtype(const AttnPartialParams& p, const CUtensorMap& map,
+                                           int grid, int nt, cudaStream_t stream) {
+  switch (nt) {
+    case 1: return launch_attention_partial_t<KVT, 1>(p, map, grid, stream);
+    case 2: return launch_attention_partial_t<KVT, 2>(p, map, grid, stream);
+    case 3: return launch_attention_partial_t<KVT, 3>(p, map, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int KVT>

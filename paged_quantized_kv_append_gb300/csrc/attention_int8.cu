@@ -13,4 +13,9 @@ int attention_blocks_per_sm_int8(int nt, int num_seqs) {
   return blocks_per_sm_dtype<PQKV_KV_INT8>(nt, num_seqs);
 }
 
+cudaError_t launch_attention_partial_int8(const AttnPartialParams& p, const CUtensorMap& map,
+                                          int grid, int nt, cudaStream_t stream) {
+  return launch_attention_partial_dtype<PQKV_KV_INT8>(p, map, grid, nt, stream);
+}
+
 }  // namespace pqkv

@@ -55,6 +55,16 @@ struct AttnParams {
   float sm_scale_log2;      // log2(e) / sqrt(head_dim)
 };
 
+// Partial mode (one rank's share of a sequence's keys, for a decode context
+// parallel split across GPUs): the keys of sequence s are its local cache;
+// query i sits at local index q_pos[s] + i; the output is O / l in fp32 and
+// the natural-log LSE m + ln l of every (query, q-head) row.
+struct AttnPartialParams : AttnParams {
+  const int32_t* q_pos;     // [B] local index of query 0's position
+  float* out_o;             // [B*q_len][Hq][128]
+  float* out_lse;           // [B*q_len][Hq]
+};
+
 // Host launchers (one per KV format), defined in the attention translation units.
 cudaError_t launch_attention_fp16(const AttnParams& p, const CUtensorMap& map, int grid,
                                   int nt, cudaStream_t stream);
@@ -70,6 +80,17 @@ int attention_blocks_per_sm_fp16(int nt, int num_seqs);
 int attention_blocks_per_sm_e4m3(int nt, int num_seqs);
 int attention_blocks_per_sm_int8(int nt, int num_seqs);
 int attention_blocks_per_sm_int8_row(int nt, int num_seqs);
+
+cudaError_t launch_attention_partial_fp16(const AttnPartialParams& p, const CUtensorMap& map,
+                                          int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_partial_e4m3(const AttnPartialParams& p, const CUtensorMap& map,
+                                          int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_partial_int8(const AttnPartialParams& p, const CUtensorMap& map,
+                                          int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_partial_int8_row(const AttnPartialParams& p, const CUtensorMap& map,
+                                              int grid, int nt, cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int num_parts,
+                             int64_t rows, uint16_t* out, float* out_lse, cudaStream_t stream);
 
 cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream);
 
