@@ -85,7 +85,7 @@ enum {
 #define PQKV_HEAD_DIM 128
 #define PQKV_PAGE_SIZE 16
 #define PQKV_MAX_Q_LEN 8
-#define PQKV_MAX_ROWS 24          /* (num_q_heads / num_kv_heads) * q_len        */
+#define PQKV_MAX_ROWS 32          /* (num_q_heads / num_kv_heads) * q_len        */
 #define PQKV_MAX_SEQS 2048
 #define PQKV_MAX_SPLITS 128
 #define PQKV_MAX_SEQ_LEN 524288   /* ReVolta README, "Performance": 512K boundary */
@@ -180,7 +180,7 @@ size_t pqkv_paged_attention_workspace_size(int32_t num_seqs, int32_t q_len,
  *                     aligned; see the counter rule above.  Calls that share a
  *                     workspace must not overlap on the device.
  * Requires head_dim == 128, page_size == 16, 1 <= q_len <= 8,
- * (num_q_heads/num_kv_heads)*q_len <= 24, num_seqs <= 2048.
+ * (num_q_heads/num_kv_heads)*q_len <= 32, num_seqs <= 2048.
  * The result does not depend on the order of pages in the pool; for a fixed
  * split mode and device it is bitwise reproducible run to run.
  */

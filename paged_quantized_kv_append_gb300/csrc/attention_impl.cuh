@@ -27,7 +27,7 @@
 //  * Math.  Four consumer warps take pages round-robin.  Per page a warp
 //    dequantises the codes in registers (exact fp16), computes S^T = K Q^T
 //    with mma.sync m16n8k16 (tokens as M, the G*q_len query rows padded to 8,
-//    16 or 24 as N), keeps an fp32 online softmax in the log2 domain whose
+//    16, 24 or 32 as N), keeps an fp32 online softmax in the log2 domain whose
 //    reference maximum is only raised when a score exceeds it by more than
 //    2^8 (so probabilities stay <= 256 in fp16), transposes P with movmatrix
 //    and accumulates O^T = V^T P^T with a second mma.  Warps merge their
@@ -48,6 +48,7 @@ struct AttnCfg {
   // flight).  Warp counts follow the register need of the row width and are
   // multiples of 4, because registers are allotted per scheduler (a quarter
   // of the SM): 8 warps get 255 registers each, 12 get 168, 16 get 128.
+  // 8 query rows (NT 1) run 16 warps, 16 rows 12, and 24 or 32 rows 8.
   static constexpr int kW = (KVT == PQKV_KV_FP16) ? 8 : (NT == 1 ? 16 : (NT == 2 ? 12 : 8));
   static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
@@ -961,6 +962,7 @@ cudaError_t launch_attention_partial_dtype(const AttnPartialParams& p, const CUt
     case 1: return launch_attention_partial_t<KVT, 1>(p, map, grid, stream);
     case 2: return launch_attention_partial_t<KVT, 2>(p, map, grid, stream);
     case 3: return launch_attention_partial_t<KVT, 3>(p, map, grid, stream);
+    case 4: return launch_attention_partial_t<KVT, 4>(p, map, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -972,6 +974,7 @@ cudaError_t launch_attention_dtype(const AttnParams& p, const CUtensorMap& map, 
     case 1: return launch_attention_t<KVT, 1>(p, map, grid, stream);
     case 2: return launch_attention_t<KVT, 2>(p, map, grid, stream);
     case 3: return launch_attention_t<KVT, 3>(p, map, grid, stream);
+    case 4: return launch_attention_t<KVT, 4>(p, map, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -982,6 +985,7 @@ int blocks_per_sm_dtype(int nt, int num_seqs) {
     case 1: return blocks_per_sm_t<KVT, 1>(num_seqs);
     case 2: return blocks_per_sm_t<KVT, 2>(num_seqs);
     case 3: return blocks_per_sm_t<KVT, 3>(num_seqs);
+    case 4: return blocks_per_sm_t<KVT, 4>(num_seqs);
     default: return 0;
   }
 }

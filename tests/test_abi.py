@@ -92,7 +92,8 @@ def test_attention_validation(lib):
     assert _attn(lib, D=256) == EUNSUPPORTED
     assert _attn(lib, hq=30) == EINVAL                    # Hq % Hkv != 0
     assert _attn(lib, qlen=9) == ERANGE
-    assert _attn(lib, qlen=7) == EUNSUPPORTED             # 4 * 7 = 28 rows > 24
+    assert _attn(lib, qlen=7) == ECUDA                    # 4 * 7 = 28 rows: supported
+    assert _attn(lib, hq=36, hkv=4, qlen=4) == EUNSUPPORTED  # 9 * 4 = 36 rows > 32
     assert _attn(lib, qlen=0) == EINVAL
     assert _attn(lib, B=0) == OK
     assert _attn(lib, B=3000) == ERANGE

@@ -66,10 +66,12 @@ def test_bitwise_deterministic_and_page_order_invariant():
     assert torch.equal(out, a)
 
 
-@pytest.mark.parametrize("kv_dtype", [W.FP16, W.FP8_E4M3, W.INT8])
-@pytest.mark.parametrize("q_len,G", [(1, 1), (1, 4), (5, 4), (1, 8), (3, 8), (8, 2), (2, 12)])
+@pytest.mark.parametrize("kv_dtype", [W.FP16, W.FP8_E4M3, W.INT8, W.INT8_ROW])
+@pytest.mark.parametrize("q_len,G", [(1, 1), (1, 4), (5, 4), (1, 8), (3, 8), (8, 2), (2, 12),
+                                     (7, 4), (8, 4), (5, 6)])
 def test_row_shapes(kv_dtype, q_len, G):
-    # every padded-row width (8, 16, 24) and ragged lengths, incl. L == q_len
+    # every padded-row width (8, 16, 24, 32) and ragged lengths, incl. L == q_len;
+    # q_len 7 and 8 with G 4 are the wider speculative verify (28 and 32 rows)
     w = W.Workload("shape", 40 + q_len * 10 + G, [q_len, 17, 100, 333], 2 * G, 2, q_len, kv_dtype,
                    outliers=kv_dtype != W.FP16, pool_slack=0.3)
     c = Case(w)

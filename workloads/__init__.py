@@ -206,6 +206,8 @@ def workload(name: str, scale: float = 1.0) -> Workload:
         return Workload(name, 6, [L(262144)] * 4, 32, 8, 1, INT8_ROW, pool_slack=0.01)
     if name == "int8_row_verify_131k":       # config 3's shapes with run-time row scales
         return Workload(name, 7, [L(131072)] * 8, 32, 8, 5, INT8_ROW, pool_slack=0.01)
+    if name == "e4m3_verify_q8_131k":        # config 3's shapes, 7 drafts + 1: 32 rows
+        return Workload(name, 8, [L(131072)] * 8, 32, 8, 8, FP8_E4M3, pool_slack=0.01)
     if name == "e4m3_verify_512k_stress":
         return Workload(name, 5, [L(524288)] * 2 + [L(32768)] * 6, 32, 8, 5, FP8_E4M3,
                         pool_slack=0.02, append_tokens=8192 if scale >= 1.0 else 520,
@@ -217,6 +219,8 @@ WORKLOAD_NAMES = ["tiny_fp16_decode", "e4m3_decode_b8", "e4m3_verify_131k",
                   "int8_decode_append_262k", "e4m3_verify_512k_stress"]
 # INT8 with run-time row scales (the pages' own INT8 design) on configs 4 and 3's shapes
 ROW_SCALED_NAMES = ["int8_row_decode_262k", "int8_row_verify_131k"]
+# the wider verify: q_len 8 (a 7-token draft), 32 query rows per kv-head
+WIDE_VERIFY_NAMES = ["e4m3_verify_q8_131k"]
 
 
 @dataclasses.dataclass
