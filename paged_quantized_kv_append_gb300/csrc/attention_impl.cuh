@@ -598,7 +598,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
       const uint32_t gi = n0 + j;
       const int stage = gi % S;
       if (!dead) {
-        bool ok = !*abort_flag && mbar_wait(&full[stage], (gi / S) & 1);
+        // one try first: the tile is usually there, and the abort flag (a
+        // shared-memory read) only matters once some wait has run out
+        bool ok = mbar_try_wait(&full[stage], (gi / S) & 1) ||
+                  (!*abort_flag && mbar_wait(&full[stage], (gi / S) & 1));
         ok = __all_sync(0xffffffffu, ok);       // keep the warp's control flow uniform
         if (!ok) {
           dead = true;
