@@ -1,5 +1,7 @@
-// Paged decode / speculative-verify attention over an FP16, E4M3 or INT8 KV
-// pool, with split-KV partitions merged by log-sum-exp.
+// Paged decode / speculative-verify attention over an FP16, E4M3, INT8 or
+// INT8-with-row-scales KV pool, with split-KV partitions merged by
+// log-sum-exp; a partial mode gives one rank's share of a decode context
+// parallel split as O / l and LSE per row.
 //
 // What it computes: ReVolta README, "Quick start" (MTP verify of 1 committed +
 // 4 draft positions with a causal mask among them, GQA) and "Weight and KV
