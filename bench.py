@@ -194,10 +194,17 @@ def algorithmic_bytes(ctx):
     return attn, app
 
 
-def kernel_source_hash():
+def kernel_source_hash(texts=None):
+    """Hash of the attention kernel's code (comments and blank lines left out,
+    so a comment edit does not orphan a capture taken on the same code)."""
+    import re
     h = hashlib.sha256()
-    for f in ("attention_impl.cuh", "pqkv_common.cuh"):
-        h.update(open(os.path.join(ROOT, "paged_quantized_kv_append_gb300", "csrc", f), "rb").read())
+    if texts is None:
+        texts = [open(os.path.join(ROOT, "paged_quantized_kv_append_gb300", "csrc", f)).read()
+                 for f in ("attention_impl.cuh", "pqkv_common.cuh")]
+    for text in texts:
+        code = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(l.rstrip() for l in code.splitlines() if l.strip()).encode())
     return h.hexdigest()[:16]
 
 
