@@ -21,6 +21,8 @@ SAMPLES = {   # workload -> sampled (sequence, kv-head) segments
     "e4m3_verify_512k_stress": [(0, 3), (5, 6)],     # a 524288-token and a 32768-token sequence
     "e4m3_verify_131k": [(4, 1)],
     "int8_decode_append_262k": [(1, 2)],
+    "e4m3_decode_b8": [(3, 5), (6, 0)],
+    "int8_row_decode_262k": [(2, 7)],
 }
 
 
@@ -30,12 +32,18 @@ def _oracle_segment(w, q, s, h, ks, vs):
     n = w.pages_of(L)
     k, v = W.kv_tokens(w, s, 0, L, "cpu", heads=[h])
     pool = oracle.new_pool(n, 1, w.head_dim, w.kv_dtype)
-    pool = oracle.kv_append_quant(k.numpy(), v.numpy(), np.arange(L, dtype=np.int64),
-                                  w.kv_dtype, [ks], [vs], pool)
+    if w.kv_dtype == W.INT8_ROW:           # scales come from the rows themselves
+        pool, ks, vs = oracle.kv_append_quant(k.numpy(), v.numpy(), np.arange(L, dtype=np.int64),
+                                              w.kv_dtype, oracle.new_scale_pool(n, 1),
+                                              oracle.new_scale_pool(n, 1), pool)
+    else:
+        pool = oracle.kv_append_quant(k.numpy(), v.numpy(), np.arange(L, dtype=np.int64),
+                                      w.kv_dtype, [ks], [vs], pool)
+        ks, vs = [ks], [vs]
     G = w.group
     rows = q[s * w.q_len:(s + 1) * w.q_len, h * G:(h + 1) * G]
     return oracle.paged_attention(rows, pool, np.arange(n, dtype=np.int32)[None, :], [L],
-                                  w.q_len, w.kv_dtype, [ks], [vs])
+                                  w.q_len, w.kv_dtype, ks, vs)
 
 
 @pytest.mark.parametrize("name", list(SAMPLES))
