@@ -79,3 +79,13 @@ def test_single_share_partial_equals_attention():
     merged = torch.empty_like(c.q)
     pq.lse_merge(o[None].contiguous(), lse[None].contiguous(), merged)
     assert torch.allclose(merged.float(), ref, rtol=1e-2, atol=2e-3)
+
+
+@pytest.mark.parametrize("num_splits", [7, 64])
+def test_shares_with_many_partitions(num_splits):
+    pq = require_gpu()
+    c = Case(W.workload("e4m3_verify_512k_stress", scale=0.004))
+    outs = _run_shares(pq, c, [(0, 50), (50, 200)], num_splits)
+    out = torch.empty_like(c.q)
+    pq.lse_merge(torch.stack([x[0] for x in outs]), torch.stack([x[1] for x in outs]), out)
+    assert_close(out, c.oracle_attention(), "many partitions %d" % num_splits)

@@ -45,6 +45,17 @@ def test_noalloc_int8_decode_and_no_split():
         assert_close(out, ref, "noalloc int8 splits %d" % ns)
 
 
+def test_noalloc_row_scaled_int8_verify():
+    pq = require_gpu()
+    c = Case(W.workload("int8_row_verify_131k", scale=0.01), with_oracle=False)
+    ref = c.attention(num_splits=0).float().cpu().numpy().astype(np.float64)
+    for call in range(2):
+        out = torch.full_like(c.q, float("nan"))
+        _noalloc(pq, c, out, 0)
+        torch.cuda.synchronize()
+        assert_close(out, ref, "noalloc int8_row call %d" % call)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     pq = require_gpu()
     # 2048 sequences x 8 kv-heads in the balanced split need more than 16 MiB
