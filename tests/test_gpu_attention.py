@@ -41,7 +41,7 @@ def test_small_workloads_match_oracle(name, num_splits):
     assert_close(out, ref, "%s splits=%d" % (name, num_splits))
 
 
-@pytest.mark.parametrize("splits", [2, 7, 64])
+@pytest.mark.parametrize("splits", [2, 7, 64, 128])     # 128: the largest split count
 def test_split_count_invariance(splits):
     c = case("e4m3_verify_512k_stress")
     a = c.attention(num_splits=1).float()
@@ -173,3 +173,32 @@ def test_host_validation_errors():
     q9 = torch.zeros((1, 9 * 8, 128), dtype=torch.float16, device="cuda")   # 72 rows per kv-head
     with pytest.raises(ValueError):
         pq.paged_attention(q9, c.pages, c.bt, c.seq_lens, 1, W.FP16, c.ks, c.vs, torch.empty_like(q9))
+
+
+def test_maximum_sequence_count():
+    # 2048 sequences, the largest batch (the per-sequence tables fill most of
+    # the shared memory): eight copies of a 256-sequence workload (the seeded
+    # generator numbers at most 256 sequences), each copy in pages of its own
+    pq = require_gpu()
+    rng = np.random.default_rng(12)
+    base = W.Workload("max_seqs", 81, rng.integers(5, 61, size=256).tolist(), 32, 8, 5,
+                      W.FP8_E4M3, pool_slack=0.05)
+    cb = Case(base)
+    ref = cb.oracle_attention()
+    big = W.Workload("max_seqs_x8", 81, base.seq_lens * 8, 32, 8, 5, W.FP8_E4M3, pool_slack=0.05)
+    plan = W.plan_pool(big)
+    pages = pq.new_pages(plan.num_pages, 8, W.FP8_E4M3, "cuda", fill=0)
+    for s2 in range(big.num_seqs):
+        L = big.seq_lens[s2]
+        k, v = W.kv_tokens(base, s2 % 256, 0, L, "cuda")
+        pq.kv_append_quant(k, v, torch.from_numpy(W.slots_for(plan, s2, 0, L)).cuda(),
+                           W.FP8_E4M3, cb.ks, cb.vs, pages)
+    q = cb.q.repeat(8, 1, 1).contiguous()
+    bt = torch.from_numpy(plan.block_table).cuda()
+    sl = torch.tensor(big.seq_lens, dtype=torch.int32, device="cuda")
+    for ns in (0, 7):
+        out = torch.empty_like(q)
+        pq.paged_attention(q, pages, bt, sl, 5, W.FP8_E4M3, cb.ks, cb.vs, out, num_splits=ns)
+        o = out.float().cpu().numpy().reshape(8, 256 * 5, 32, 128)
+        for copy in range(8):
+            assert_close(o[copy], ref, "2048 sequences copy %d splits=%d" % (copy, ns))
