@@ -127,3 +127,23 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
             pq.load_library(str(tmp_path / "missing.so"))
         finally:
             pq._lib = pq._lib_saved
+
+
+def _declared_params():
+    """{function: number of parameters} from the header's prototypes."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"#define[^\n]*", "", text)
+    out = {}
+    for m in re.finditer(r"\b(pqkv_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    declared = _declared_params()
+    assert set(declared) == set(declared_functions())
+    for name, n in declared.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
