@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged quantized-KV attention: effective KV GB/s (% of HBM peak), µs/step"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+REFERENCE_BUDGET_S = 90.0     # host time of the whole --impl reference run
 
 
 def parse_args():
@@ -241,66 +242,95 @@ def cpu_threads():
         return len(os.sched_getaffinity(0))
 
 
-def oracle_sample(wname: str, seconds: float, max_segments: int = 64):
-    """Time the oracle's paged attention over (sequence, kv-head) segments of
-    a 32768-token sequence of the workload until `seconds` have elapsed."""
-    import numpy as np
-    import oracle
-    import workloads as W
+class OracleSample:
+    """One (sequence, kv-head) segment of the workload -- its shortest
+    sequence, up to 32768 tokens -- encoded once by the oracle; run(n) times
+    the oracle's paged attention over the first n tokens of it."""
 
-    w = W.workload(wname)
-    plan = W.plan_pool(w)
-    s = int(np.argmin(w.seq_lens))
-    L = w.seq_lens[s]
-    n = w.pages_of(L)
-    rng = np.random.default_rng(0)
-    bt = rng.permutation(n).astype(np.int32)[None, :]
-    k, v = W.kv_tokens(w, s, 0, L, "cpu")
-    kscale = W.scale_from_amax(k.float().abs().max().item(), 448.0)
-    vscale = W.scale_from_amax(v.float().abs().max().item(), 448.0)
-    t = np.arange(L)
-    pool = oracle.new_pool(n, w.num_kv_heads, w.head_dim, w.kv_dtype)
-    pool = oracle.kv_append_quant(k.numpy(), v.numpy(), bt[0, t // 16].astype(np.int64) * 16 + t % 16,
-                                  w.kv_dtype, [kscale], [vscale], pool)
-    q = W.query(w, "cpu").numpy()[s * w.q_len:(s + 1) * w.q_len]
-    done, seg_bytes = 0, L * w.head_dim * 2 * w.elem_bytes
+    def __init__(self, wname: str):
+        import numpy as np
+        import oracle
+        import workloads as W
+        self.oracle, self.np = oracle, np
+        w = W.workload(wname)
+        self.w = w
+        s = int(np.argmin(w.seq_lens))
+        self.L = L = w.seq_lens[s]
+        n = w.pages_of(L)
+        rng = np.random.default_rng(0)
+        self.bt = rng.permutation(n).astype(np.int32)[None, :]
+        k, v = W.kv_tokens(w, s, 0, L, "cpu")
+        self.ks = W.scale_from_amax(k.float().abs().max().item(), 448.0)
+        self.vs = W.scale_from_amax(v.float().abs().max().item(), 448.0)
+        t = np.arange(L)
+        pool = oracle.new_pool(n, w.num_kv_heads, w.head_dim, w.kv_dtype)
+        self.pool = oracle.kv_append_quant(k.numpy(), v.numpy(),
+                                           self.bt[0, t // 16].astype(np.int64) * 16 + t % 16,
+                                           w.kv_dtype, [self.ks], [self.vs], pool)
+        self.q = W.query(w, "cpu").numpy()[s * w.q_len:(s + 1) * w.q_len]
+        self.h = 0
+
+    def run(self, n_tokens: int):
+        """(KV code bytes read, seconds) of one oracle call over n_tokens keys."""
+        w = self.w
+        n = max(w.q_len, min(int(n_tokens), self.L))
+        t0 = time.perf_counter()
+        self.oracle.paged_attention(self.q, self.pool, self.bt, [n], w.q_len, w.kv_dtype,
+                                    [self.ks], [self.vs], heads=[self.h])
+        dt = time.perf_counter() - t0
+        self.h = (self.h + 1) % w.num_kv_heads
+        return n * w.head_dim * 2 * w.elem_bytes, dt
+
+    def describe(self, n):
+        w = self.w
+        return ("oracle paged_attention (float64 numpy) over (sequence, kv-head) segments of %d "
+                "tokens (q_len %d, %d query rows each) of the workload's %d-token sequences; KV code "
+                "bytes read / wall time" % (n, w.q_len, w.group * w.q_len, self.L))
+
+
+def oracle_sample(wname: str, seconds: float, max_segments: int = 64):
+    """Time the oracle on whole segments of the workload's shortest sequence
+    until `seconds` have elapsed (at least one segment)."""
+    smp = OracleSample(wname)
+    done, nbytes = 0, 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds and done < max_segments:
-        h = done % w.num_kv_heads
-        oracle.paged_attention(q, pool, bt, [L], w.q_len, w.kv_dtype, [kscale], [vscale],
-                               heads=[h])
+        b, _ = smp.run(smp.L)
+        nbytes += b
         done += 1
     dt = time.perf_counter() - t0
-    return {"value": done * seg_bytes / dt / 1e9, "unit": UNIT, "cores": cpu_threads(),
-            "kind": "oracle",
-            "sample": "oracle paged_attention (float64 numpy) over %d (sequence, kv-head) segments "
-                      "of %d tokens (q_len %d, %d query rows each) of the workload; KV code "
-                      "bytes read / wall time" % (done, L, w.q_len, w.group * w.q_len),
-            "seconds": dt}
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": "%d segments: " % done + smp.describe(smp.L), "seconds": dt}
 
 
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    workload: every step runs the oracle over the first n tokens of one
+    (sequence, kv-head) segment, n chosen from a calibration so that all
+    warm-up and timed steps fit about REFERENCE_BUDGET_S seconds."""
     if rank != 0:
         return
-    import numpy as np
-    steps = []
-    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    last = None
-    for i in range(args.warmup + args.steps):
-        r = oracle_sample(args.workload, per_step, max_segments=8)
-        if i >= args.warmup:
-            steps.append(r)
-        last = r
-    value = statistics.median([r["value"] for r in steps])
-    sec = statistics.median([r["seconds"] for r in steps])
-    cb = dict(last)
-    cb["value"] = value
+    smp = OracleSample(args.workload)
+    b0, t0 = smp.run(min(smp.L, 2048))                      # calibration
+    per_token = t0 / max(1, min(smp.L, 2048))
+    per_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    n = int(max(256, min(smp.L, per_step / max(per_token, 1e-9))))
+    for _ in range(args.warmup):
+        smp.run(n)
+    tot_b, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        b, dt = smp.run(n)
+        tot_b += b
+        tot_s += dt
+    value = tot_b / tot_s / 1e9
+    cb = {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+          "sample": "%d steps, each: " % args.steps + smp.describe(n), "seconds": tot_s}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": tot_s * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "sample": cb["sample"]},
             "cpu_baseline": cb,
