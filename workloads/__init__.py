@@ -202,11 +202,11 @@ def workload(name: str, scale: float = 1.0) -> Workload:
     if name == "int8_decode_append_262k":
         return Workload(name, 4, [L(262144)] * 4, 32, 8, 1, INT8, scale_per_head=True,
                         pool_slack=0.01, append_per_step=1)
-    if name == "int8_row_decode_262k":       # config 4's shapes with run-time row scales
+    if name == "int8_row_decode_262k":       # the 262K INT8 decode's shapes, run-time row scales
         return Workload(name, 6, [L(262144)] * 4, 32, 8, 1, INT8_ROW, pool_slack=0.01)
-    if name == "int8_row_verify_131k":       # config 3's shapes with run-time row scales
+    if name == "int8_row_verify_131k":       # the 131K E4M3 verify's shapes, run-time row scales
         return Workload(name, 7, [L(131072)] * 8, 32, 8, 5, INT8_ROW, pool_slack=0.01)
-    if name == "e4m3_verify_q8_131k":        # config 3's shapes, 7 drafts + 1: 32 rows
+    if name == "e4m3_verify_q8_131k":        # the 131K verify with 7 drafts + 1: 32 rows
         return Workload(name, 8, [L(131072)] * 8, 32, 8, 8, FP8_E4M3, pool_slack=0.01)
     if name == "e4m3_verify_512k_stress":
         return Workload(name, 5, [L(524288)] * 2 + [L(32768)] * 6, 32, 8, 5, FP8_E4M3,
@@ -217,7 +217,8 @@ def workload(name: str, scale: float = 1.0) -> Workload:
 
 WORKLOAD_NAMES = ["tiny_fp16_decode", "e4m3_decode_b8", "e4m3_verify_131k",
                   "int8_decode_append_262k", "e4m3_verify_512k_stress"]
-# INT8 with run-time row scales (the pages' own INT8 design) on configs 4 and 3's shapes
+# INT8 with run-time row scales (the README's own INT8 design) on the 262K decode's and
+# the 131K verify's shapes
 ROW_SCALED_NAMES = ["int8_row_decode_262k", "int8_row_verify_131k"]
 # the wider verify: q_len 8 (a 7-token draft), 32 query rows per kv-head
 WIDE_VERIFY_NAMES = ["e4m3_verify_q8_131k"]
