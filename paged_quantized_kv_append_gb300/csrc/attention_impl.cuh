@@ -20,20 +20,22 @@
 //    writes an unnormalised partial (O, m, l) and the last block to finish a
 //    segment (an atomic ticket; no block ever waits on another) merges the
 //    partials in a fixed order.
-//  * Data movement.  One producer warp streams the (page, kv-head) tiles --
-//    16 K rows followed by 16 V rows, 4 KB for 8-bit codes -- with 4-D TMA
-//    loads (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared
-//    memory stages guarded by mbarriers.  Block-table entries are read 32 at
-//    a time by the whole warp, one batch ahead.  Out-of-range page ids read
+//  * Data movement.  Every warp feeds itself: the block's pages are dealt
+//    round-robin to its warps, and each warp streams its own (page, kv-head)
+//    tiles -- 16 K rows followed by 16 V rows, 4 KB for 8-bit codes -- with
+//    4-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle) into ring stages
+//    that only it uses, each guarded by an mbarrier; a stage is refilled as
+//    soon as its warp has read it.  A warp's lanes look up the pool pages of
+//    its next 32 tiles at once, one batch ahead.  Out-of-range page ids read
 //    as zeros (TMA bounds) and are reported.
-//  * Math.  Four consumer warps take pages round-robin.  Per page a warp
-//    dequantises the codes in registers (exact fp16), computes S^T = K Q^T
-//    with mma.sync m16n8k16 (tokens as M, the G*q_len query rows padded to 8,
-//    16, 24 or 32 as N), keeps an fp32 online softmax in the log2 domain whose
-//    reference maximum is only raised when a score exceeds it by more than
-//    2^8 (so probabilities stay <= 256 in fp16), transposes P with movmatrix
-//    and accumulates O^T = V^T P^T with a second mma.  Warps merge their
-//    states through shared memory at the end of each segment share.
+//  * Math.  Per page a warp dequantises the codes in registers (exact fp16),
+//    computes S^T = K Q^T with mma.sync m16n8k16 (tokens as M, the G*q_len
+//    query rows padded to 8, 16, 24 or 32 as N), keeps an fp32 online softmax
+//    in the log2 domain whose reference maximum is only raised when a score
+//    exceeds it by more than 2^8 (so probabilities stay <= 256 in fp16),
+//    transposes P with movmatrix and accumulates O^T = V^T P^T with a second
+//    mma.  Warps merge their states through shared memory at the end of each
+//    segment share.
 #pragma once
 
 #include "pqkv_common.cuh"
