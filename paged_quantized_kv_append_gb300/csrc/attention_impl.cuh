@@ -80,7 +80,12 @@ struct AttnCfg {
   static constexpr int kScBytes = kRowScaled ? kStages * 128 : 0;
   static constexpr int kBarOff = kScOff + kScBytes;
   static constexpr int kMiscOff = kBarOff + kStages * 8;
-  static constexpr int kMiscBytes = 64 + kW * 4 + 2 * kRP * 4 + 128;
+  // 32 query rows (NT 4) are short of registers: there the per-row causal
+  // limits live in shared memory and the rescale test recomputes its
+  // threshold from the reference maximum instead of keeping it per row
+  // (fewer spills; with fewer rows the registers are faster)
+  static constexpr bool kRowsInSmem = (NT == 4);
+  static constexpr int kMiscBytes = 64 + kW * 4 + 2 * kRP * 4 + 128 + (kRowsInSmem ? kRP * 4 : 0);
   static constexpr int kPreOff = kMiscOff + kMiscBytes;
   static __host__ __device__ constexpr int smem_bytes(int num_seqs) {
     return kPreOff + (2 * num_seqs + 1) * 4 + 1024;
@@ -370,6 +375,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   FragIter* sit = reinterpret_cast<FragIter*>(sLrow + RP);
   Frag* sf = reinterpret_cast<Frag*>(sit + 1);
   int* pre = reinterpret_cast<int*>(smem + Cfg::kPreOff);
+  int* sLim = reinterpret_cast<int*>(smem + Cfg::kPreOff - RP * 4);   // [RP] if kRowsInSmem
   int* slen = pre + p.num_seqs + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -568,13 +574,19 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
       inv_qk_scale = 1.f / qk_scale;
       if constexpr (kPartial) lim_min = p.q_pos[f_s];
       else lim_min = L - p.q_len;
+      // causal limit per row: the last key position row r may see
+      if constexpr (Cfg::kRowsInSmem) {
+        for (int r = tid; r < RP; r += nthr)
+          sLim[r] = r < p.rows ? lim_min + r / p.group : 0x7fffffff;
+      } else {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int r = 8 * nt + 2 * t + c;
-          lim[nt][c] = r < p.rows ? lim_min + r / p.group : 0x7fffffff;
-        }
+          for (int c = 0; c < 2; ++c) {
+            const int r = 8 * nt + 2 * t + c;
+            lim[nt][c] = r < p.rows ? lim_min + r / p.group : 0x7fffffff;
+          }
+      }
       cur_seg = f_seg;
       cur_L = L;
       __syncthreads();
@@ -588,7 +600,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         mref[nt][c] = kNoScore;
-        thr[nt][c] = (kNoScore + 8.f) * inv_qk_scale;
+        if constexpr (!Cfg::kRowsInSmem) thr[nt][c] = (kNoScore + 8.f) * inv_qk_scale;
         lsum[nt][c] = 0.f;
       }
 #pragma unroll
@@ -646,19 +658,25 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = pos0 + g + ((e & 2) ? 8 : 0);
-            if (tok > lim[nt][e & 1]) sc[nt][e] = -INFINITY;
+            const int lm = Cfg::kRowsInSmem ? sLim[8 * nt + 2 * t + (e & 1)] : lim[nt][e & 1];
+            if (tok > lm) sc[nt][e] = -INFINITY;
           }
       }
       // The reference maximum of a row only moves when one of its scores
       // exceeds it by more than 8 (probabilities then stay <= 2^8).  Each lane
-      // tests its own raw scores against thr = (mref + 8) / qk_scale; only
-      // then does the warp form the exact page maximum across the 8 lanes
-      // that share a row and rescale.
+      // tests its own raw scores against thr = (mref + 8) / qk_scale (with 32
+      // rows: raw * qk_scale - mref against 8); only then does the warp form
+      // the exact page maximum across the 8 lanes that share a row and
+      // rescale.
       bool raise = false;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) raise |= fmaxf(sc[nt][c], sc[nt][c + 2]) > thr[nt][c];
+        for (int c = 0; c < 2; ++c) {
+          const float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
+          if constexpr (Cfg::kRowsInSmem) raise |= fmaf(mx, qk_scale, -mref[nt][c]) > 8.f;
+          else raise |= mx > thr[nt][c];
+        }
       if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -672,7 +690,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
             if (m > mref[nt][c] + 8.f) {
               const float fct = ex2(mref[nt][c] - m);
               mref[nt][c] = m;
-              thr[nt][c] = (m + 8.f) * inv_qk_scale;
+              if constexpr (!Cfg::kRowsInSmem) thr[nt][c] = (m + 8.f) * inv_qk_scale;
               lsum[nt][c] *= fct;
 #pragma unroll
               for (int mt = 0; mt < 8; ++mt) {
