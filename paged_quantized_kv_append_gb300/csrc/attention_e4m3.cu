@@ -1,6 +1,6 @@
 // Paged attention instantiations for one KV format (kept in its own
 // translation unit so the formats compile in parallel).
-#include "attention_impl.cuh"
+#include "attention_launch.cuh"
 
 namespace pqkv {
 

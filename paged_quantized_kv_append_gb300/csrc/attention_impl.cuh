@@ -924,95 +924,4 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------
-template <int KVT, int NT>
-cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& map, int grid,
-                               cudaStream_t stream) {
-  using Cfg = AttnCfg<KVT, NT>;
-  static bool attr_set = false;
-  const int smem = Cfg::smem_bytes(p.num_seqs);
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<KVT, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::smem_bytes(PQKV_MAX_SEQS));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  paged_attention_kernel<KVT, NT><<<grid, Cfg::kThreads, smem, stream>>>(map, p);
-  return cudaGetLastError();
-}
-
-template <int KVT, int NT>
-int blocks_per_sm_t(int num_seqs) {
-  using Cfg = AttnCfg<KVT, NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(paged_attention_kernel<KVT, NT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::smem_bytes(PQKV_MAX_SEQS)) != cudaSuccess)
-      return 0;
-    attr_set = true;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<KVT, NT>,
-                                                    Cfg::kThreads,
-                                                    Cfg::smem_bytes(num_seqs)) != cudaSuccess)
-    return 0;
-  return n;
-}
-
-template <int KVT, int NT>
-cudaError_t launch_attention_partial_t(const AttnPartialParams& p, const CUtensorMap& map,
-                                       int grid, cudaStream_t stream) {
-  using Cfg = AttnCfg<KVT, NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<KVT, NT, AttnPartialParams>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::smem_bytes(PQKV_MAX_SEQS));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  paged_attention_kernel<KVT, NT, AttnPartialParams>
-      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
-  return cudaGetLastError();
-}
-
-template <int KVT>
-cudaError_t launch_attention_partial_dtype(const AttnPartialParams& p, const CUtensorMap& map,
-                                           int grid, int nt, cudaStream_t stream) {
-  switch (nt) {
-    case 1: return launch_attention_partial_t<KVT, 1>(p, map, grid, stream);
-    case 2: return launch_attention_partial_t<KVT, 2>(p, map, grid, stream);
-    case 3: return launch_attention_partial_t<KVT, 3>(p, map, grid, stream);
-    case 4: return launch_attention_partial_t<KVT, 4>(p, map, grid, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int KVT>
-cudaError_t launch_attention_dtype(const AttnParams& p, const CUtensorMap& map, int grid, int nt,
-                                   cudaStream_t stream) {
-  switch (nt) {
-    case 1: return launch_attention_t<KVT, 1>(p, map, grid, stream);
-    case 2: return launch_attention_t<KVT, 2>(p, map, grid, stream);
-    case 3: return launch_attention_t<KVT, 3>(p, map, grid, stream);
-    case 4: return launch_attention_t<KVT, 4>(p, map, grid, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int KVT>
-int blocks_per_sm_dtype(int nt, int num_seqs) {
-  switch (nt) {
-    case 1: return blocks_per_sm_t<KVT, 1>(num_seqs);
-    case 2: return blocks_per_sm_t<KVT, 2>(num_seqs);
-    case 3: return blocks_per_sm_t<KVT, 3>(num_seqs);
-    case 4: return blocks_per_sm_t<KVT, 4>(num_seqs);
-    default: return 0;
-  }
-}
-
 }  // namespace pqkv
