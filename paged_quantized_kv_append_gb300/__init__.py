@@ -106,6 +106,21 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _on_device(dev, **tensors):
+    """Every tensor the kernels read or write must live on the pool's GPU: a
+    host or other-device pointer would be dereferenced on the device."""
+    for name, x in tensors.items():
+        if x is not None and (not x.is_cuda or x.device != dev):
+            raise ValueError("%s must be a CUDA tensor on %s, got %s" % (name, dev, x.device))
+
+
+def _check_status(status, dev):
+    if status is not None:
+        _on_device(dev, status=status)
+        if status.dtype != torch.int32 or status.numel() < 1:
+            raise ValueError("status must be an int32 CUDA tensor of at least one element")
+
+
 def _dtype_id(kv_dtype) -> int:
     if isinstance(kv_dtype, str):
         return KV_DTYPES[kv_dtype]
@@ -189,11 +204,16 @@ def kv_append_quant(k, v, slot_mapping, kv_dtype, k_scale, v_scale, pages, statu
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
+    dev = pages.device
+    _on_device(dev, k=k, v=v, slot_mapping=slot_mapping, k_scale=k_scale if kd in _SCALED else None,
+               v_scale=v_scale if kd in _SCALED else None)
+    _check_status(status, dev)
     lib = load_library()
-    rc = lib.pqkv_kv_append_quant(
-        _ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), T, H, HEAD_DIM, kd,
-        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
-        _ptr(pages), pages.shape[0], PAGE_SIZE, _ptr(status), _stream(pages, stream))
+    with torch.cuda.device(dev):
+        rc = lib.pqkv_kv_append_quant(
+            _ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), T, H, HEAD_DIM, kd,
+            _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None),
+            sph, _ptr(pages), pages.shape[0], PAGE_SIZE, _ptr(status), _stream(pages, stream))
     _check(rc, "kv_append_quant")
     return pages
 
@@ -261,17 +281,24 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
+    dev = pages.device
+    _on_device(dev, q=q, out=out, block_table=block_table, seq_lens=seq_lens,
+               k_scale=k_scale if kd in _SCALED else None,
+               v_scale=v_scale if kd in _SCALED else None)
+    _check_status(status, dev)
     need = workspace_size(B, q_len, Hq, H, num_splits)
     if workspace is None:
-        workspace = _default_workspace(q.device)
+        workspace = _default_workspace(dev)
     ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    _on_device(dev, workspace=ws)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     lib = load_library()
-    rc = lib.pqkv_paged_attention(
-        _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
-        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
-        num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
+    with torch.cuda.device(dev):
+        rc = lib.pqkv_paged_attention(
+            _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
+            _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None),
+            sph, num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention")
     return out
 
@@ -308,17 +335,25 @@ def paged_attention_partial(q, pages, block_table, seq_lens, q_pos, q_len, kv_dt
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
+    dev = pages.device
+    _on_device(dev, q=q, out_o=out_o, out_lse=out_lse, block_table=block_table,
+               seq_lens=seq_lens, q_pos=q_pos, k_scale=k_scale if kd in _SCALED else None,
+               v_scale=v_scale if kd in _SCALED else None)
+    _check_status(status, dev)
     need = workspace_size(B, q_len, Hq, H, num_splits)
     if workspace is None:
-        workspace = _default_workspace(q.device)
+        workspace = _default_workspace(dev)
     ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    _on_device(dev, workspace=ws)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    rc = load_library().pqkv_paged_attention_partial(
-        _ptr(q), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), _ptr(q_pos), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
-        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
-        num_splits, max_seq_len, _ptr(out_o), _ptr(out_lse), _ptr(ws), ws_bytes, _ptr(status),
-        _stream(q, stream))
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.pqkv_paged_attention_partial(
+            _ptr(q), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
+            _ptr(seq_lens), _ptr(q_pos), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
+            _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None),
+            sph, num_splits, max_seq_len, _ptr(out_o), _ptr(out_lse), _ptr(ws), ws_bytes,
+            _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention_partial")
     return out_o, out_lse
 
@@ -337,8 +372,12 @@ def lse_merge(parts_o, parts_lse, out, out_lse=None, stream=None):
         raise ValueError("out must be contiguous fp16 with rows * 128 elements")
     if out_lse is not None and (out_lse.dtype != torch.float32 or out_lse.numel() != rows):
         raise ValueError("out_lse must be fp32 with one value per row")
-    rc = load_library().pqkv_lse_merge(_ptr(parts_o), _ptr(parts_lse), P, rows, HEAD_DIM,
-                                       _ptr(out), _ptr(out_lse), _stream(out, stream))
+    dev = out.device
+    _on_device(dev, parts_o=parts_o, parts_lse=parts_lse, out=out, out_lse=out_lse)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.pqkv_lse_merge(_ptr(parts_o), _ptr(parts_lse), P, rows, HEAD_DIM, _ptr(out),
+                                _ptr(out_lse), _stream(out, stream))
     _check(rc, "lse_merge")
     return out
 
@@ -373,11 +412,19 @@ def paged_attention_noalloc(q, pages, block_table, seq_lens, q_len, kv_dtype, k_
         sph = _check_scale(k_scale, H, "k_scale")
         if _check_scale(v_scale, H, "v_scale") != sph:
             raise ValueError("k_scale and v_scale must have the same shape")
-    rc = load_library().pqkv_paged_attention_noalloc(
-        _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), B, q_len, q.shape[1], H, HEAD_DIM, PAGE_SIZE, kd,
-        _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None), sph,
-        num_splits, max_seq_len, _ptr(status), _stream(q, stream))
+    dev = pages.device
+    _on_device(dev, q=q, out=out, block_table=block_table, seq_lens=seq_lens,
+               k_scale=k_scale if kd in _SCALED else None,
+               v_scale=v_scale if kd in _SCALED else None)
+    _check_status(status, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.pqkv_paged_attention_noalloc(
+            _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), B, q_len, q.shape[1], H, HEAD_DIM, PAGE_SIZE,
+            kd, _ptr(k_scale if kd in _SCALED else None),
+            _ptr(v_scale if kd in _SCALED else None), sph, num_splits, max_seq_len, _ptr(status),
+            _stream(q, stream))
     _check(rc, "paged_attention_noalloc")
     return out
 

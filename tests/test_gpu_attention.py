@@ -175,6 +175,42 @@ def test_host_validation_errors():
         pq.paged_attention(q9, c.pages, c.bt, c.seq_lens, 1, W.FP16, c.ks, c.vs, torch.empty_like(q9))
 
 
+def test_host_tensors_rejected():
+    # a host tensor's pointer must never reach a kernel: each entry point
+    # refuses it before launching anything
+    pq = require_gpu()
+    c = case("e4m3_verify_131k")
+    w = c.w
+    out = torch.empty_like(c.q)
+    args = dict(q=c.q, bt=c.bt, seq_lens=c.seq_lens, ks=c.ks, vs=c.vs, out=out)
+    for name in args:
+        bad = dict(args)
+        bad[name] = args[name].cpu()
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            pq.paged_attention(bad["q"], c.pages, bad["bt"], bad["seq_lens"], w.q_len, w.kv_dtype,
+                               bad["ks"], bad["vs"], bad["out"])
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            pq.paged_attention_noalloc(bad["q"], c.pages, bad["bt"], bad["seq_lens"], w.q_len,
+                                       w.kv_dtype, bad["ks"], bad["vs"], bad["out"])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pq.paged_attention(c.q, c.pages, c.bt, c.seq_lens, w.q_len, w.kv_dtype, c.ks, c.vs, out,
+                           status=torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pq.paged_attention(c.q, c.pages, c.bt, c.seq_lens, w.q_len, w.kv_dtype, c.ks, c.vs, out,
+                           workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+    k = torch.zeros((4, w.num_kv_heads, 128), dtype=torch.float16, device="cuda")
+    slots = torch.arange(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pq.kv_append_quant(k, k, slots, w.kv_dtype, c.ks, c.vs, c.pages)
+    o = torch.zeros((2, 3, 128), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((2, 3), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pq.lse_merge(o, lse, torch.empty((3, 128), dtype=torch.float16, device="cuda"))
+    # nothing was launched with a bad pointer: the pool still gives the oracle's answer
+    assert_close(pq.paged_attention(c.q, c.pages, c.bt, c.seq_lens, w.q_len, w.kv_dtype, c.ks,
+                                    c.vs, out), c.oracle_attention(), "after the rejected calls")
+
+
 def test_maximum_sequence_count():
     # 2048 sequences, the largest batch (the per-sequence tables fill most of
     # the shared memory): eight copies of a 256-sequence workload (the seeded
