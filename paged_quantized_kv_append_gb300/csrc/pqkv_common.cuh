@@ -165,10 +165,17 @@ __device__ __forceinline__ uint32_t i8pair(uint32_t t) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// INT8: 4 codes of a word -> (d0,d1), (d2,d3)
+// INT8: 4 codes of a word -> (d0,d1), (d2,d3).  The sign bits are flipped
+// once for the whole word; one byte permute per pair then places two codes
+// under the exponent byte 0x64 (1024 + (c + 128)), and 1152 is subtracted.
 __device__ __forceinline__ void int8_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  lo = i8pair(__byte_perm(w, 0, 0x0100));
-  hi = i8pair(__byte_perm(w, 0, 0x0302));
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t l = __byte_perm(x, 0x64646464u, 0x4140), h = __byte_perm(x, 0x64646464u, 0x4342);
+  const __half2 off = __half2(__half(1152.0f), __half(1152.0f));
+  __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&l), off);
+  __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&h), off);
+  lo = *reinterpret_cast<uint32_t*>(&hl);
+  hi = *reinterpret_cast<uint32_t*>(&hh);
 }
 
 }  // namespace pqkv

@@ -135,6 +135,48 @@ def test_every_e4m3_code_in_k_and_v():
     assert_close(out, ref, "all codes")
 
 
+@pytest.mark.parametrize("kv_dtype", [W.INT8, W.INT8_ROW])
+@pytest.mark.parametrize("q_len", [1, 5])
+def test_every_int8_code_in_k_and_v(kv_dtype, q_len):
+    # every byte value (-128 .. 127; append never writes -128, the widening
+    # must still be exact) at many (token, dim) places of K and V, for both
+    # 8-bit integer formats and both row widths (8 and 24 padded query rows)
+    pq = require_gpu()
+    L, num_pages = 64, 4
+    rng = np.random.default_rng(7 + q_len)
+    pool = np.zeros((num_pages, 1, 2, 16, 128), np.uint8)
+    base = np.tile(np.arange(256, dtype=np.uint8), 64).reshape(L, 2, 128)
+    tok = rng.permuted(base.reshape(-1)).reshape(L, 2, 128)   # each value exactly 64 times
+    for j in range(L):
+        pool[j // 16, 0, 0, j % 16] = tok[j, 0]
+        pool[j // 16, 0, 1, j % 16] = tok[j, 1]
+    G = 4
+    # scores spread over a few units, so that a wrong K code moves the output
+    q = torch.from_numpy(rng.normal(0, 0.5, (q_len, G, 128)).astype(np.float16)).cuda()
+    bt = torch.tensor([[0, 1, 2, 3]], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    if kv_dtype == W.INT8:
+        pages = torch.from_numpy(pool).cuda()
+        ks = torch.tensor([0.05], dtype=torch.float32, device="cuda")
+        vs = torch.tensor([0.03], dtype=torch.float32, device="cuda")
+        pq.paged_attention(q, pages, bt, sl, q_len, kv_dtype, ks, vs, out)
+        ref = oracle.paged_attention(q.cpu().numpy(), pool, bt.cpu().numpy(), [L], q_len,
+                                     kv_dtype, [0.05], [0.03])
+    else:
+        pages = pq.new_pages(num_pages, 1, W.INT8_ROW, "cuda", fill=0)
+        pages.copy_(torch.from_numpy(pool))
+        kp = rng.uniform(0.02, 0.08, (num_pages, 1, 16)).astype(np.float32)
+        vp = rng.uniform(0.01, 0.05, (num_pages, 1, 16)).astype(np.float32)
+        sc = pq.row_scales(pages)
+        sc[:, :, 0].copy_(torch.from_numpy(kp))
+        sc[:, :, 1].copy_(torch.from_numpy(vp))
+        pq.paged_attention(q, pages, bt, sl, q_len, kv_dtype, None, None, out)
+        ref = oracle.paged_attention(q.cpu().numpy(), pool, bt.cpu().numpy(), [L], q_len,
+                                     kv_dtype, kp, vp)
+    assert_close(out, ref, "all int8 codes, format %d, q_len %d" % (kv_dtype, q_len))
+
+
 def test_stale_nan_codes_past_the_end_are_ignored():
     pq = require_gpu()
     w = W.Workload("nan_tail", 77, [37, 50], 8, 2, 5, W.FP8_E4M3, pool_slack=0.5)
