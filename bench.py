@@ -181,17 +181,23 @@ def setup(wname: str, device: str, scale: float = 1.0):
     if w.append_tokens:
         ctx["ak"], ctx["av"] = W.append_chunk(w, device)
         ctx["aslots"] = torch.from_numpy(plan.append_slots).to(device)
+    elif w.append_per_step:
+        ctx["ak"], ctx["av"], sl = W.step_tokens(w, plan, device)
+        ctx["aslots"] = torch.from_numpy(sl).to(device)
     ctx["ws"] = pq.Workspace(device)
     torch.cuda.synchronize()
     return ctx
 
 
 def algorithmic_bytes(ctx):
+    import workloads as W
+
     w = ctx["w"]
     B, H = w.num_seqs, w.num_kv_heads
     attn = (w.kv_bytes() + 2 * ctx["q"].numel() * 2
             + sum(w.pages_of(L) for L in w.seq_lens) * 4 + B * 4)
-    app = w.append_bytes(w.append_tokens) if w.append_tokens else 0
+    n = W.step_append_tokens(w)
+    app = w.append_bytes(n) if n else 0
     return attn, app
 
 
@@ -341,6 +347,7 @@ def run_reference(args, rank, world):
 def run_pqkv(args, rank, local, world):
     import torch
     import paged_quantized_kv_append_gb300 as pq
+    import workloads as W
     from paged_quantized_kv_append_gb300 import build as pqbuild
 
     pqbuild.build()
@@ -351,10 +358,11 @@ def run_pqkv(args, rank, local, world):
     w = ctx["w"]
     stream = torch.cuda.current_stream()
     attn_bytes, app_bytes = algorithmic_bytes(ctx)
-    launches_per_step = 1 + (1 if w.append_tokens else 0)
+    appends = "ak" in ctx
+    launches_per_step = 1 + (1 if appends else 0)
 
     def step(ev=None):
-        if w.append_tokens:
+        if appends:
             pq.kv_append_quant(ctx["ak"], ctx["av"], ctx["aslots"], w.kv_dtype, ctx["ks"],
                                ctx["vs"], ctx["pages"])
         if ev is not None:
@@ -428,7 +436,7 @@ def run_pqkv(args, rank, local, world):
     #      step i computes (two buffer sets), the usual serving pipeline.
     e2e = None
     if not args.no_e2e:
-        names = ["q", "bt", "seq_lens"] + (["ak", "av", "aslots"] if w.append_tokens else [])
+        names = ["q", "bt", "seq_lens"] + (["ak", "av", "aslots"] if appends else [])
         host = {n: ctx[n].cpu().pin_memory() for n in names}
         dev_in = [{n: torch.empty_like(ctx[n]) for n in names} for _ in range(2)]
         outs = [torch.empty_like(ctx["out"]) for _ in range(2)]
@@ -452,7 +460,7 @@ def run_pqkv(args, rank, local, world):
                     d[n].copy_(t, non_blocking=True)
                 ev_copied[b].record(copy_stream)
             stream.wait_event(ev_copied[b])
-            if w.append_tokens:
+            if appends:
                 pq.kv_append_quant(d["ak"], d["av"], d["aslots"], w.kv_dtype, ctx["ks"],
                                    ctx["vs"], ctx["pages"])
             pq.paged_attention(d["q"], ctx["pages"], d["bt"], d["seq_lens"], w.q_len, w.kv_dtype,
@@ -504,7 +512,7 @@ def run_pqkv(args, rank, local, world):
                    "seq_lens": "2x524288+6x32768" if (w.name.endswith("stress") and args.scale == 1.0)
                    else w.seq_lens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "page_size": w.page_size, "q_len": w.q_len,
-                   "append_tokens": w.append_tokens, "num_splits": args.num_splits,
+                   "append_tokens": W.step_append_tokens(w), "num_splits": args.num_splits,
                    "attention_bytes": attn_bytes, "append_bytes": app_bytes,
                    "l2": "inputs larger than L2 (%.2f GB of KV per step)" % (w.kv_bytes() / 1e9)},
         "roofline": {"bound": "hbm", "kernel": "paged_attention_kernel", "achieved": achieved,

@@ -82,3 +82,20 @@ def test_scales_follow_amax():
     amax0 = max(W.kv_tokens(w, s, 0, L)[0][:, 0].float().abs().max().item()
                 for s, L in enumerate(w.seq_lens))
     assert ks[0].item() == np.float32(amax0 / 127.0)
+
+
+def test_decode_step_tokens_are_the_newest_of_each_sequence():
+    # the INT8 decode step appends one token per sequence: the last one of
+    # each sequence, at the slot the block table gives it
+    w = W.workload("int8_decode_append_262k", scale=0.004)
+    plan = W.plan_pool(w)
+    k, v, slots = W.step_tokens(w, plan)
+    B, H = w.num_seqs, w.num_kv_heads
+    assert k.shape == v.shape == (B, H, 128) and slots.shape == (B,)
+    assert W.step_append_tokens(w) == B
+    for s, L in enumerate(w.seq_lens):
+        kk, vv = W.kv_tokens(w, s, L - 1, L)
+        assert torch.equal(k[s], kk[0]) and torch.equal(v[s], vv[0])
+        assert slots[s] == plan.block_table[s, (L - 1) // 16] * 16 + (L - 1) % 16
+    stress = W.workload("e4m3_verify_512k_stress")
+    assert W.step_append_tokens(stress) == 8192

@@ -294,6 +294,28 @@ def append_chunk(w: Workload, device="cpu"):
     return k, v
 
 
+def step_tokens(w: Workload, plan: PoolPlan, device="cpu"):
+    """The decode step's own append, ``append_per_step`` tokens per sequence:
+    the newest tokens of every sequence (the ones its query sees last), as
+    fp16 K and V [B * n, Hkv, D] with their slots int64 [B * n].  They are the
+    values the pool already holds at those slots, so re-appending them every
+    step is idempotent and a timed loop stays in steady state."""
+    n = w.append_per_step
+    ks, vs, sl = [], [], []
+    for s, L in enumerate(w.seq_lens):
+        k, v = kv_tokens(w, s, L - n, L, device)
+        ks.append(k)
+        vs.append(v)
+        sl.append(slots_for(plan, s, L - n, L))
+    return torch.cat(ks).contiguous(), torch.cat(vs).contiguous(), np.concatenate(sl)
+
+
+def step_append_tokens(w: Workload) -> int:
+    """Tokens one timed step appends: the extra chunk, or the decode step's
+    own tokens."""
+    return w.append_tokens or w.num_seqs * w.append_per_step
+
+
 def calibrated_scales(w: Workload, device="cpu"):
     """Per-layer (or per-kv-head for INT8) scales: amax of the layer's fp16 K
     (resp. V) over every cached token, divided by the format's largest value.
