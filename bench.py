@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the CUDA-graph replay timing of the same step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload figures (every workload at full size and the "
+                         "8192-token append, about a minute)")
     return ap.parse_args()
 
 
@@ -139,19 +142,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples_in_timed_region": len(sm),
                 "samples_total": total}
 
-    def stop(self, t_start, t_end):
+    def window(self, t_start, t_end):
+        """Summary of the samples inside [t_start, t_end] (host wall time)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        r = self.summarize(self.path, t_start, t_end)
+        r["window_s"] = round(t_end - t_start, 4)
+        return r
+
+    def close(self):
+        if self.proc is None:
+            return
         time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        r = self.summarize(self.path, t_start, t_end)
-        r["window_s"] = round(t_end - t_start, 4)
-        os.unlink(self.path)
-        return r
+
+    def remove(self):
+        if self.path and os.path.exists(self.path):
+            os.unlink(self.path)
 
 
 # ---------------------------------------------------------------------------
@@ -239,13 +250,19 @@ def hbm_peak():
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample
 # ---------------------------------------------------------------------------
-def cpu_threads():
+def cpu_cores():
+    """Host cores this process may run on (its CPU affinity)."""
+    return len(os.sched_getaffinity(0))
+
+
+def blas_threads():
+    """Threads of the BLAS / OpenMP pools numpy runs the oracle's products on
+    (the largest pool), or None when it cannot be queried."""
     try:
         from threadpoolctl import threadpool_info
-        n = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-        return n
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except Exception:
-        return len(os.sched_getaffinity(0))
+        return None
 
 
 class OracleSample:
@@ -305,8 +322,226 @@ def oracle_sample(wname: str, seconds: float, max_segments: int = 64):
         nbytes += b
         done += 1
     dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cpu_cores(),
+            "blas_threads": blas_threads(), "kind": "oracle",
             "sample": "%d segments: " % done + smp.describe(smp.L), "seconds": dt}
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+LOAD_S = 0.6          # seconds of identical load before and after the headline's timed steps
+CONFIG_MIN_S = 1.0    # each per-config figure is timed over at least this much wall time
+
+
+def run_for(fn, seconds):
+    """Run fn back to back for about `seconds` of wall time, keeping at most
+    two batches queued so the GPU never idles for long."""
+    import torch
+    prev = None
+    t_end = time.time() + seconds
+    while time.time() < t_end:
+        for _ in range(8):
+            fn()
+        ev = torch.cuda.Event()
+        ev.record()
+        if prev is not None:
+            prev.synchronize()
+        prev = ev
+    torch.cuda.synchronize()
+
+
+def graph_time(fns, reps, min_s):
+    """Capture `reps` passes over fns in one CUDA graph, replay it back to
+    back for at least min_s seconds, and return (us per pass, (t0, t1)) from
+    CUDA events around the replays on the current stream."""
+    import math
+    import torch
+    stream = torch.cuda.current_stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            for f in fns:
+                f()
+    g.replay()
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    g.replay()
+    torch.cuda.synchronize()
+    one = time.perf_counter() - c0
+    n = max(3, int(math.ceil(min_s / max(one, 1e-6))))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(n):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    del g
+    return e0.elapsed_time(e1) * 1e3 / (n * reps), (t0, t1)
+
+
+def reps_for(fn, target_s=2e-3, cap=200):
+    """Passes per graph so that one replay lasts about target_s."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    per = e0.elapsed_time(e1) * 1e-3 / 5
+    return max(1, min(cap, int(target_s / max(per, 1e-7))))
+
+
+class L2Flush:
+    """Reads a buffer twice the size of L2 (a read leaves no dirty lines for
+    the next kernel to write back)."""
+
+    def __init__(self, device):
+        import torch
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.buf = torch.ones(max(1, 2 * l2 // 4), dtype=torch.float32, device=device)
+        self.l2 = l2
+
+    def __call__(self):
+        self.buf.sum()
+
+
+def _span(windows):
+    return min(a for a, _ in windows), max(b for _, b in windows)
+
+
+def _rate(nbytes, us, peak):
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_step": us, "gbs": gbs, "frac_of_hbm": gbs / peak}
+
+
+def config_entry(pq, W, ctx, peak, flush=None, headline=None):
+    """One workload's figures: the step (append if the workload appends every
+    step, then attention) and the attention alone, each a CUDA graph of
+    back-to-back launches replayed for at least CONFIG_MIN_S; with `flush`,
+    also the same launches after an L2 flush (flush + launch minus flush)."""
+    w = ctx["w"]
+    attn_bytes, app_bytes = algorithmic_bytes(ctx)
+    step_appends = bool(w.append_per_step) or bool(w.append_tokens)
+
+    def attention():
+        pq.paged_attention(ctx["q"], ctx["pages"], ctx["bt"], ctx["seq_lens"], w.q_len,
+                           w.kv_dtype, ctx["ks"], ctx["vs"], ctx["out"], workspace=ctx["ws"],
+                           max_seq_len=max(w.seq_lens))
+
+    def append():
+        pq.kv_append_quant(ctx["ak"], ctx["av"], ctx["aslots"], w.kv_dtype, ctx["ks"], ctx["vs"],
+                           ctx["pages"])
+
+    step = [append, attention] if step_appends else [attention]
+    windows = []
+    reps = reps_for(lambda: [f() for f in step])
+    step_us, win = graph_time(step, reps, CONFIG_MIN_S)
+    windows.append(win)
+    if step_appends:
+        attn_us, win = graph_time([attention], reps, CONFIG_MIN_S / 2)
+        windows.append(win)
+    else:
+        attn_us = step_us
+    e = {"workload": w.name,
+         "shape": "%s x %s tokens, %d/%d heads, q_len %d, %s" % (
+             w.num_seqs, (w.seq_lens[0] if len(set(w.seq_lens)) == 1 else
+                          "%d..%d" % (min(w.seq_lens), max(w.seq_lens))),
+             w.num_q_heads, w.num_kv_heads, w.q_len,
+             {0: "fp16", 1: "e4m3", 2: "int8", 3: "int8 row scales"}[w.kv_dtype]),
+         "step": ("append %d tokens + attention" % W.step_append_tokens(w)) if step_appends
+         else "attention",
+         "attention_bytes": attn_bytes, "append_bytes": app_bytes if step_appends else 0,
+         "l2": "warm: back-to-back launches on the same inputs" if flush else
+               "inputs larger than L2 (%.2f GB of KV)" % (w.kv_bytes() / 1e9)}
+    e.update(_rate(attn_bytes + (app_bytes if step_appends else 0), step_us, peak))
+    e["attention_us"] = attn_us
+    e["attention_frac_of_hbm"] = attn_bytes / (attn_us * 1e-6) / 1e9 / peak
+    if headline is not None:
+        e["bench_line_attention_us"] = headline
+    if flush is not None:
+        f_reps = max(1, min(reps, 50))
+        both_us, win = graph_time([flush] + step, f_reps, CONFIG_MIN_S / 2)
+        windows.append(win)
+        fl_us, win = graph_time([flush], f_reps, CONFIG_MIN_S / 2)
+        windows.append(win)
+        us = both_us - fl_us
+        e["l2_flushed"] = dict(_rate(attn_bytes, us, peak),
+                               how="each launch after a read of %d MB (2x L2): graph of "
+                                   "(read, launch) minus graph of (read)" % (2 * flush.l2 >> 20))
+    e["_win"] = _span(windows)
+    e["timing"] = ("CUDA graph of %d back-to-back steps replayed for >= %.1f s, CUDA events "
+                   "around the replays" % (reps, CONFIG_MIN_S))
+    return e
+
+
+def append_entry(pq, W, device, peak, ks, vs, n_sets=6):
+    """The 8192-token append of the long-context stress workload on its own:
+    n_sets copies of the chunk, each into its own fragmented set of free pages
+    (offset 7 inside the first), cycled so the inputs and written pages
+    (6 x 50 MB) exceed L2."""
+    import numpy as np
+    import torch
+    w = W.workload("e4m3_verify_512k_stress")
+    npg = w.pages_of(w.append_tokens + w.append_offset)
+    rng = np.random.default_rng(np.random.SeedSequence([w.seed, 9]))
+    num_pages = n_sets * npg + 64
+    perm = rng.permutation(num_pages).astype(np.int64)
+    pages = pq.new_pages(num_pages, w.num_kv_heads, w.kv_dtype, device, fill=0)
+    ak, av = W.append_chunk(w, device)
+    t = np.arange(w.append_tokens, dtype=np.int64) + w.append_offset
+    sets = []
+    for i in range(n_sets):
+        chunk = perm[i * npg:(i + 1) * npg]
+        sl = torch.from_numpy(chunk[t // 16] * 16 + t % 16).to(device)
+        sets.append((ak.clone(), av.clone(), sl))
+
+    def one(i):
+        k, v, sl = sets[i]
+        return lambda: pq.kv_append_quant(k, v, sl, w.kv_dtype, ks, vs, pages)
+
+    fns = [one(i) for i in range(n_sets)]
+    reps = reps_for(lambda: [f() for f in fns])
+    us, win = graph_time(fns, reps, CONFIG_MIN_S)
+    us /= n_sets
+    nbytes = w.append_bytes(w.append_tokens)
+    e = {"workload": "append_8192_fragmented",
+         "shape": "8192 tokens x 8 kv-heads, E4M3, into a fragmented pool at page offset 7",
+         "append_bytes": nbytes, "l2": "%d rotating input/page sets (%.0f MB) > L2" % (
+             n_sets, n_sets * nbytes / 1e6)}
+    e.update(_rate(nbytes, us, peak))
+    e["_win"] = win
+    e["timing"] = "CUDA graph of %d x %d appends replayed for >= %.1f s" % (reps, n_sets,
+                                                                          CONFIG_MIN_S)
+    del pages, sets
+    return e
+
+
+def per_config(pq, W, device, peak, headline_ctx, headline_us):
+    """Every workload of the path at full size, plus the 8192-token append."""
+    import gc
+    import torch
+    out = {}
+    flush = L2Flush(device)
+    out[headline_ctx["w"].name] = config_entry(pq, W, headline_ctx, peak, headline=headline_us)
+    for name in ("tiny_fp16_decode", "e4m3_decode_b8", "e4m3_verify_131k",
+                 "int8_decode_append_262k"):
+        ctx = setup(name, device)
+        small = ctx["w"].kv_bytes() < 2 * flush.l2
+        out[name] = config_entry(pq, W, ctx, peak, flush=flush if small else None)
+        del ctx
+        gc.collect()
+        torch.cuda.empty_cache()
+    out["append_8192_fragmented"] = append_entry(pq, W, device, peak, headline_ctx["ks"],
+                                                 headline_ctx["vs"])
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -332,7 +567,8 @@ def run_reference(args, rank, world):
         tot_b += b
         tot_s += dt
     value = tot_b / tot_s / 1e9
-    cb = {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+    cb = {"value": value, "unit": UNIT, "cores": cpu_cores(), "blas_threads": blas_threads(),
+          "kind": "oracle",
           "sample": "%d steps, each: " % args.steps + smp.describe(n), "seconds": tot_s}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -378,13 +614,19 @@ def run_pqkv(args, rank, local, world):
         step()
     torch.cuda.synchronize()
 
-    # ---- device-timed region
+    # ---- device-timed region: exactly --steps steps between a barrier and a
+    #      synchronize on each side.  The clock record covers a load window of
+    #      identical back-to-back steps around it (LOAD_S before and after), so
+    #      the 100 ms nvidia-smi samples fall under the same load even when the
+    #      timed region itself is shorter than one sampling interval.
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
     attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    load_start = time.time()
+    run_for(step, LOAD_S)
     barrier(world)
     torch.cuda.synchronize()
     w_start = time.time()
@@ -395,7 +637,9 @@ def run_pqkv(args, rank, local, world):
     torch.cuda.synchronize()
     w_end = time.time()
     barrier(world)
-    clk = clocks.stop(w_start, w_end)
+    run_for(step, LOAD_S)
+    torch.cuda.synchronize()
+    load_end = time.time()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = total_ms / args.steps
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
@@ -496,9 +740,22 @@ def run_pqkv(args, rank, local, world):
                "pipeline": "step i+1's inputs copied on a second stream while step i computes; "
                            "each step's output copied back and read on the host"}
 
+    peak, peak_src = hbm_peak()
+    configs = None
+    if not args.no_per_config and args.scale == 1.0 and args.workload == "e4m3_verify_512k_stress":
+        configs = per_config(pq, W, dev, peak, ctx, attn_avg * 1e3)
+    clocks.close()
+    clk = clocks.window(load_start, load_end)
+    clk["window"] = ("load window: the timed steps with %.1f s of the same back-to-back steps "
+                     "before and after" % LOAD_S)
+    clk["samples_in_timed_steps"] = clocks.window(w_start, w_end)["samples_in_timed_region"]
+    clk["timed_steps_s"] = round(w_end - w_start, 4)
+    if configs:
+        for e in configs.values():
+            e["clocks"] = clocks.window(*e.pop("_win"))
+    clocks.remove()
     if rank != 0:
         return
-    peak, peak_src = hbm_peak()
     achieved = attn_bytes / (attn_avg * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -524,6 +781,7 @@ def run_pqkv(args, rank, local, world):
         "clocks": clk,
         "e2e": e2e,
         "graph": graph,
+        "per_config": configs,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(args.workload, args.cpu_seconds)

@@ -31,8 +31,11 @@
  *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers owned by the caller.  Nothing
- *     is allocated, freed or retained; the library keeps no state between
- *     calls except a per-device cache of device properties.
+ *     is allocated, freed or retained.  Between calls the library keeps only
+ *     a per-device cache of device properties, and -- the one exception --
+ *     the scratch area of pqkv_paged_attention_noalloc (a file-scope device
+ *     array present on every GPU that loads the library, its per-device
+ *     address cache and the last call's contents; see that entry point).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  The return value reports argument validation and
  *     launch errors only.
@@ -256,16 +259,25 @@ int pqkv_lse_merge(const float* part_o, const float* part_lse, int32_t num_parts
  * the library uses its own fixed scratch area of PQKV_NOALLOC_SCRATCH_BYTES, a
  * file-scope device array.  Nothing is allocated or freed, by the library or by
  * any routine it calls.
- *   - Returns PQKV_ERANGE when pqkv_paged_attention_workspace_size() for these
- *     sizes exceeds PQKV_NOALLOC_SCRATCH_BYTES (num_splits == 1 needs none).
- *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *   - Returns PQKV_ERANGE when the workspace of the launch this call makes
+ *     exceeds PQKV_NOALLOC_SCRATCH_BYTES.  That is the grid the call actually
+ *     uses, not the largest one pqkv_paged_attention_workspace_size() assumes:
+ *     with RP = (num_q_heads/num_kv_heads)*q_len rounded up to a multiple of
+ *     8, it needs PQKV_COUNTER_BYTES(num_seqs, num_kv_heads) plus about
+ *     n*RP*520 bytes, where n = num_seqs*num_kv_heads*num_splits for
+ *     num_splits >= 2, and n = num_seqs*num_kv_heads + G for num_splits == 0,
+ *     G the balanced grid (at most the blocks resident on the device at once:
+ *     one per SM in this build); num_splits == 1 needs none.
+ *   - All arguments are checked before anything is queued: a rejected call
+ *     leaves the scratch area untouched.
+ *   - The first call on a device that needs scratch looks up the array's
+ *     device address (cudaGetSymbolAddress) with that device current; make
+ *     that first call before any stream capture begins.
  *   - Every call on a device shares the one scratch area and it keeps the last
  *     call's contents; each call clears the part that must start at zero
- *     (cudaMemsetAsync on `stream`).  Calls that overlap on the GPU (different
- *     streams, or concurrent host threads) race on it and must be serialised by
- *     the caller.
+ *     (cudaMemsetAsync on `stream`, queued just before the kernel).  Calls that
+ *     overlap on the GPU (different streams, or concurrent host threads) race
+ *     on it and must be serialised by the caller.
  */
 int pqkv_paged_attention_noalloc(const void* q, void* out, const void* pages, int64_t num_pages,
                                  const int32_t* block_table, int32_t max_pages_per_seq,
@@ -279,7 +291,9 @@ int pqkv_paged_attention_noalloc(const void* q, void* out, const void* pages, in
 #define PQKV_COUNTER_BYTES(num_seqs, num_kv_heads) \
   ((((size_t)(num_seqs) * (size_t)(num_kv_heads) * 4u) + 255u) & ~(size_t)255u)
 
-/* Static description of a return code or of a device status word. */
+/* Static description of a return code, or of a device status word holding any
+ * combination of OR-ed PQKV_DEV_* bits ("device: a; b"); "unknown status" for
+ * anything else.  The returned string lives until the process exits. */
 const char* pqkv_status_string(int code);
 
 /* Library version as "major.minor.patch". */

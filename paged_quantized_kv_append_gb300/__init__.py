@@ -392,7 +392,8 @@ def paged_attention_noalloc(q, pages, block_table, seq_lens, q_len, kv_dtype, k_
 
     The first call on a device must come before any stream capture; calls on
     one device share the scratch area and must not overlap on the GPU.
-    Raises ValueError when the sizes need more scratch than the area holds.
+    Raises ValueError when the launch this call makes needs more scratch than
+    the area holds (include/pqkv.h states the sizes).
     """
     kd = _dtype_id(kv_dtype)
     _check_pages(pages, kd)
@@ -402,9 +403,11 @@ def paged_attention_noalloc(q, pages, block_table, seq_lens, q_len, kv_dtype, k_
     if out.shape != q.shape or out.dtype != torch.float16 or not out.is_contiguous():
         raise ValueError("out must be contiguous fp16 shaped like q")
     B = seq_lens.shape[0]
-    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32 or \
-            block_table.shape[0] != B or not block_table.is_contiguous():
-        raise ValueError("seq_lens / block_table must be int32 with one row per sequence")
+    if seq_lens.dtype != torch.int32 or seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be int32 [num_seqs]")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous int32 [num_seqs, max_pages_per_seq]")
     if q.shape[0] != B * q_len:
         raise ValueError("q has %d rows, expected num_seqs*q_len = %d" % (q.shape[0], B * q_len))
     sph = 0

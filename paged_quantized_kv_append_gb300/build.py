@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpqkv.so")
 SOURCES = ["api.cu", "append.cu", "attention_fp16.cu", "attention_e4m3.cu", "attention_int8.cu",
-           "attention_int8row.cu", "merge.cu", "noalloc.cu"]
+           "attention_int8row.cu", "attention_waittest.cu", "merge.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

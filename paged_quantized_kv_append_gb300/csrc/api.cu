@@ -6,6 +6,8 @@
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -79,13 +81,6 @@ int blocks_per_sm(int kv_dtype, int nt, int num_seqs) {
   }
   return 0;
 }
-
-// Sizes shared by the workspace query and the launch.
-struct AttnPlan {
-  int rows = 0, rp = 0, nt = 0;
-  int64_t slots = 0;        // partial-result slots
-  size_t counter_bytes = 0, o_bytes = 0, ml_bytes = 0, total = 0;
-};
 
 int plan_attention(int32_t num_seqs, int32_t q_len, int32_t hq, int32_t hkv, int32_t num_splits,
                    int grid, AttnPlan* pl) {
@@ -167,8 +162,11 @@ extern "C" int pqkv_kv_append_quant(const void* k, int64_t k_token_stride, const
   p.row_scales = kv_dtype == PQKV_KV_INT8_ROW ? row_scale_area(pages, num_pages, num_kv_heads)
                                               : nullptr;
   p.status = status;
+  // one pass when the chunk fits the resident threads (8 blocks of 256 per
+  // SM, two vectors per thread), grid-stride beyond that
   const int64_t work = (int64_t)num_tokens * num_kv_heads * (kHeadDim / 16);
-  const int64_t blocks = (work + 255) / 256;
+  const int64_t per_block = (int64_t)kAppendThreads * kAppendUnroll;
+  const int64_t blocks = (work + per_block - 1) / per_block;
   const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * 8);
   if (launch_append(p, kv_dtype, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PQKV_ECUDA;
@@ -187,56 +185,56 @@ extern "C" size_t pqkv_paged_attention_workspace_size(int32_t num_seqs, int32_t 
 }
 
 namespace pqkv {
-namespace {
 
-// Validation, grid, workspace plan and TMA map shared by the attention entry
-// points; fills everything in *p except the output pointer.
-int prepare_attention(const void* q, const void* pages, int64_t num_pages,
-                      const int32_t* block_table, int32_t max_pages_per_seq,
-                      const int32_t* seq_lens, int32_t num_seqs, int32_t q_len,
-                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                      int32_t page_size, int32_t kv_dtype, const float* k_scale,
-                      const float* v_scale, int32_t scale_per_head, int32_t num_splits,
-                      int32_t max_seq_len, void* workspace, size_t workspace_bytes,
-                      int32_t* status, AttnParams* pp, CUtensorMap* mapp, int* gridp, int* ntp) {
-  int rc = validate_common(head_dim, page_size, kv_dtype);
+int plan_attention_launch(const AttnArgs& a, AttnLaunch* L) {
+  int rc = validate_common(a.head_dim, a.page_size, a.kv_dtype);
   if (rc) return rc;
-  rc = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
+  rc = validate_heads(a.num_seqs, a.q_len, a.num_q_heads, a.num_kv_heads);
   if (rc) return rc;
-  if (num_splits < 0 || num_splits > PQKV_MAX_SPLITS) return PQKV_ERANGE;
-  if (num_seqs == 0) return PQKV_OK;
-  if (!q || !pages || !block_table || !seq_lens) return PQKV_EINVAL;
-  if (uses_scale_args(kv_dtype) && (!k_scale || !v_scale)) return PQKV_EINVAL;
-  if (num_pages < 1 || num_pages > INT32_MAX || max_pages_per_seq < 1) return PQKV_EINVAL;
-  if ((int64_t)max_pages_per_seq * page_size > PQKV_MAX_SEQ_LEN + page_size) return PQKV_ERANGE;
-  if (max_seq_len < 0) return PQKV_EINVAL;
-  if (!aligned(q, 16) || !aligned(pages, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+  if (a.num_splits < 0 || a.num_splits > PQKV_MAX_SPLITS) return PQKV_ERANGE;
+  if (a.num_seqs == 0) return PQKV_OK;
+  if (!a.q || !a.pages || !a.block_table || !a.seq_lens) return PQKV_EINVAL;
+  if (uses_scale_args(a.kv_dtype) && (!a.k_scale || !a.v_scale)) return PQKV_EINVAL;
+  if (a.num_pages < 1 || a.num_pages > INT32_MAX || a.max_pages_per_seq < 1) return PQKV_EINVAL;
+  if ((int64_t)a.max_pages_per_seq * a.page_size > PQKV_MAX_SEQ_LEN + a.page_size)
+    return PQKV_ERANGE;
+  if (a.max_seq_len < 0) return PQKV_EINVAL;
+  if (!aligned(a.q, 16) || !aligned(a.pages, 16) || !aligned(a.block_table, 4) ||
+      !aligned(a.seq_lens, 4))
     return PQKV_EINVAL;
   int sms = 0;
   rc = current_device_sms(&sms);
   if (rc) return rc;
-  AttnPlan pl;
-  const int rows = (num_q_heads / num_kv_heads) * q_len;
+  const int rows = (a.num_q_heads / a.num_kv_heads) * a.q_len;
   const int nt = rows_padded(rows) / 8;
 
   // grid
   int grid;
-  if (num_splits == 0) {
-    const int per_sm = blocks_per_sm(kv_dtype, nt, num_seqs);
+  if (a.num_splits == 0) {
+    const int per_sm = blocks_per_sm(a.kv_dtype, nt, a.num_seqs);
     if (per_sm <= 0) return PQKV_ECUDA;
-    const int64_t lmax = max_seq_len > 0 ? std::min<int64_t>(max_seq_len,
-                                                             (int64_t)max_pages_per_seq * page_size)
-                                         : (int64_t)max_pages_per_seq * page_size;
-    const int64_t units = (int64_t)num_seqs * num_kv_heads * ((lmax + page_size - 1) / page_size);
+    const int64_t cap_len = (int64_t)a.max_pages_per_seq * a.page_size;
+    const int64_t lmax = a.max_seq_len > 0 ? std::min<int64_t>(a.max_seq_len, cap_len) : cap_len;
+    const int64_t units =
+        (int64_t)a.num_seqs * a.num_kv_heads * ((lmax + a.page_size - 1) / a.page_size);
     const int64_t want = (units + kMinPagesPerBlock - 1) / kMinPagesPerBlock;
     const int64_t cap = std::min<int64_t>((int64_t)sms * per_sm, (int64_t)kMaxGrid);
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
   } else {
-    const int64_t g = (int64_t)num_seqs * num_kv_heads * num_splits;
+    const int64_t g = (int64_t)a.num_seqs * a.num_kv_heads * a.num_splits;
     if (g > INT32_MAX) return PQKV_ERANGE;
     grid = (int)g;
   }
-  plan_attention(num_seqs, q_len, num_q_heads, num_kv_heads, num_splits, grid, &pl);
+  plan_attention(a.num_seqs, a.q_len, a.num_q_heads, a.num_kv_heads, a.num_splits, grid, &L->pl);
+  L->grid = grid;
+  L->nt = nt;
+  L->rows = rows;
+  return PQKV_OK;
+}
+
+int bind_attention(const AttnArgs& a, const AttnLaunch& L, void* workspace,
+                   size_t workspace_bytes, int32_t* status, AttnParams* pp, CUtensorMap* mapp) {
+  const AttnPlan& pl = L.pl;
   if (pl.total > 0) {
     if (!workspace) return PQKV_EWORKSPACE;
     if (!aligned(workspace, 256) || workspace_bytes < pl.total) return PQKV_EWORKSPACE;
@@ -245,32 +243,32 @@ int prepare_attention(const void* q, const void* pages, int64_t num_pages,
   // TMA map over the pool: [num_pages][Hkv][lines][128 bytes]
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return PQKV_ECUDA;
-  const int eb = elem_bytes(kv_dtype);
-  const cuuint32_t lines = (cuuint32_t)(2 * page_size * head_dim * eb / 128);
+  const int eb = elem_bytes(a.kv_dtype);
+  const cuuint32_t lines = (cuuint32_t)(2 * a.page_size * a.head_dim * eb / 128);
   CUtensorMap& map = *mapp;
   std::memset(&map, 0, sizeof(map));
-  const cuuint64_t dims[4] = {(cuuint64_t)(128 / eb), lines, (cuuint64_t)num_kv_heads,
-                              (cuuint64_t)num_pages};
+  const cuuint64_t dims[4] = {(cuuint64_t)(128 / eb), lines, (cuuint64_t)a.num_kv_heads,
+                              (cuuint64_t)a.num_pages};
   const cuuint64_t strides[3] = {128, (cuuint64_t)lines * 128,
-                                 (cuuint64_t)lines * 128 * num_kv_heads};
+                                 (cuuint64_t)lines * 128 * a.num_kv_heads};
   const cuuint32_t box[4] = {(cuuint32_t)(128 / eb), lines, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult cr = enc(&map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                          4, const_cast<void*>(pages), dims, strides, box, estr,
+                          4, const_cast<void*>(a.pages), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return PQKV_ECUDA;
 
   AttnParams& p = *pp;
-  p.q = static_cast<const uint16_t*>(q);
+  p.q = static_cast<const uint16_t*>(a.q);
   p.out = nullptr;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
   // INT8_ROW reads no scale arguments: its k_scale slot carries the row-scale area
-  p.k_scale = kv_dtype == PQKV_KV_INT8_ROW
-                  ? row_scale_area(const_cast<void*>(pages), num_pages, num_kv_heads)
-                  : k_scale;
-  p.v_scale = v_scale;
+  p.k_scale = a.kv_dtype == PQKV_KV_INT8_ROW
+                  ? row_scale_area(const_cast<void*>(a.pages), a.num_pages, a.num_kv_heads)
+                  : a.k_scale;
+  p.v_scale = a.v_scale;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = pl.total ? reinterpret_cast<int32_t*>(ws) : nullptr;
   p.part_o = pl.total ? reinterpret_cast<float*>(ws + pl.counter_bytes) : nullptr;
@@ -278,24 +276,40 @@ int prepare_attention(const void* q, const void* pages, int64_t num_pages,
                                                   ((pl.o_bytes + 255) & ~size_t(255)))
                        : nullptr;
   p.status = status;
-  p.num_pages = num_pages;
-  p.bt_stride = max_pages_per_seq;
-  p.num_seqs = num_seqs;
-  p.q_len = q_len;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.group = num_q_heads / num_kv_heads;
-  p.rows = rows;
-  p.scale_per_head = scale_per_head ? 1 : 0;
-  p.num_splits = num_splits;
-  p.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
-
-  *gridp = grid;
-  *ntp = nt;
+  p.num_pages = a.num_pages;
+  p.bt_stride = a.max_pages_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.q_len = a.q_len;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.rows = L.rows;
+  p.scale_per_head = a.scale_per_head ? 1 : 0;
+  p.num_splits = a.num_splits;
+  p.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a.head_dim));
   return PQKV_OK;
 }
 
-}  // namespace
+cudaError_t launch_attention(int kv_dtype, const AttnParams& p, const CUtensorMap& map, int grid,
+                             int nt, cudaStream_t st) {
+  switch (kv_dtype) {
+    case PQKV_KV_FP16: return launch_attention_fp16(p, map, grid, nt, st);
+    case PQKV_KV_FP8_E4M3: return launch_attention_e4m3(p, map, grid, nt, st);
+    case PQKV_KV_INT8_ROW: return launch_attention_int8_row(p, map, grid, nt, st);
+    default: return launch_attention_int8(p, map, grid, nt, st);
+  }
+}
+
+int check_output_args(const AttnArgs& a, bool bad_outputs) {
+  if (a.num_seqs > 0 && bad_outputs) {
+    const int rc0 = validate_common(a.head_dim, a.page_size, a.kv_dtype);
+    if (rc0) return rc0;
+    const int rc1 = validate_heads(a.num_seqs, a.q_len, a.num_q_heads, a.num_kv_heads);
+    return rc1 ? rc1 : PQKV_EINVAL;
+  }
+  return PQKV_OK;
+}
+
 }  // namespace pqkv
 
 extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
@@ -307,29 +321,21 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
                                     int32_t scale_per_head, int32_t num_splits,
                                     int32_t max_seq_len, void* workspace, size_t workspace_bytes,
                                     int32_t* status, void* stream) {
-  if (num_seqs > 0 && (!out || !aligned(out, 16))) {
-    const int rc0 = validate_common(head_dim, page_size, kv_dtype);
-    if (rc0) return rc0;
-    const int rc1 = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
-    return rc1 ? rc1 : PQKV_EINVAL;
-  }
+  const AttnArgs a{q, pages, num_pages, block_table, max_pages_per_seq, seq_lens, num_seqs, q_len,
+                   num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype, k_scale, v_scale,
+                   scale_per_head, num_splits, max_seq_len};
+  int rc = check_output_args(a, !out || !aligned(out, 16));
+  if (rc) return rc;
+  AttnLaunch L;
+  rc = plan_attention_launch(a, &L);
+  if (rc || num_seqs == 0) return rc;
   AttnParams p;
   CUtensorMap map;
-  int grid = 0, nt = 0;
-  int rc = prepare_attention(q, pages, num_pages, block_table, max_pages_per_seq, seq_lens,
-                             num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
-                             kv_dtype, k_scale, v_scale, scale_per_head, num_splits, max_seq_len,
-                             workspace, workspace_bytes, status, &p, &map, &grid, &nt);
-  if (rc || num_seqs == 0) return rc;
+  rc = bind_attention(a, L, workspace, workspace_bytes, status, &p, &map);
+  if (rc) return rc;
   p.out = static_cast<uint16_t*>(out);
-  cudaError_t e;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  switch (kv_dtype) {
-    case PQKV_KV_FP16: e = launch_attention_fp16(p, map, grid, nt, st); break;
-    case PQKV_KV_FP8_E4M3: e = launch_attention_e4m3(p, map, grid, nt, st); break;
-    case PQKV_KV_INT8_ROW: e = launch_attention_int8_row(p, map, grid, nt, st); break;
-    default: e = launch_attention_int8(p, map, grid, nt, st); break;
-  }
+  const cudaError_t e =
+      launch_attention(kv_dtype, p, map, L.grid, L.nt, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }
 
@@ -340,31 +346,29 @@ extern "C" int pqkv_paged_attention_partial(
     int32_t kv_dtype, const float* k_scale, const float* v_scale, int32_t scale_per_head,
     int32_t num_splits, int32_t max_seq_len, float* out_o, float* out_lse, void* workspace,
     size_t workspace_bytes, int32_t* status, void* stream) {
-  if (num_seqs > 0 && (!q_pos || !out_o || !out_lse || !aligned(q_pos, 4) ||
-                       !aligned(out_o, 16) || !aligned(out_lse, 4))) {
-    const int rc0 = validate_common(head_dim, page_size, kv_dtype);
-    if (rc0) return rc0;
-    const int rc1 = validate_heads(num_seqs, q_len, num_q_heads, num_kv_heads);
-    return rc1 ? rc1 : PQKV_EINVAL;
-  }
+  const AttnArgs a{q, pages, num_pages, block_table, max_pages_per_seq, seq_lens, num_seqs, q_len,
+                   num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype, k_scale, v_scale,
+                   scale_per_head, num_splits, max_seq_len};
+  int rc = check_output_args(a, !q_pos || !out_o || !out_lse || !aligned(q_pos, 4) ||
+                                    !aligned(out_o, 16) || !aligned(out_lse, 4));
+  if (rc) return rc;
+  AttnLaunch L;
+  rc = plan_attention_launch(a, &L);
+  if (rc || num_seqs == 0) return rc;
   AttnPartialParams p;
   CUtensorMap map;
-  int grid = 0, nt = 0;
-  int rc = prepare_attention(q, pages, num_pages, block_table, max_pages_per_seq, seq_lens,
-                             num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
-                             kv_dtype, k_scale, v_scale, scale_per_head, num_splits, max_seq_len,
-                             workspace, workspace_bytes, status, &p, &map, &grid, &nt);
-  if (rc || num_seqs == 0) return rc;
+  rc = bind_attention(a, L, workspace, workspace_bytes, status, &p, &map);
+  if (rc) return rc;
   p.q_pos = q_pos;
   p.out_o = out_o;
   p.out_lse = out_lse;
   cudaError_t e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (kv_dtype) {
-    case PQKV_KV_FP16: e = launch_attention_partial_fp16(p, map, grid, nt, st); break;
-    case PQKV_KV_FP8_E4M3: e = launch_attention_partial_e4m3(p, map, grid, nt, st); break;
-    case PQKV_KV_INT8_ROW: e = launch_attention_partial_int8_row(p, map, grid, nt, st); break;
-    default: e = launch_attention_partial_int8(p, map, grid, nt, st); break;
+    case PQKV_KV_FP16: e = launch_attention_partial_fp16(p, map, L.grid, L.nt, st); break;
+    case PQKV_KV_FP8_E4M3: e = launch_attention_partial_e4m3(p, map, L.grid, L.nt, st); break;
+    case PQKV_KV_INT8_ROW: e = launch_attention_partial_int8_row(p, map, L.grid, L.nt, st); break;
+    default: e = launch_attention_partial_int8(p, map, L.grid, L.nt, st); break;
   }
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }
@@ -385,6 +389,46 @@ extern "C" int pqkv_lse_merge(const float* part_o, const float* part_lse, int32_
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }
 
+namespace pqkv {
+namespace {
+
+constexpr int kDevBits = 5;   // PQKV_DEV_SLOT_RANGE .. PQKV_DEV_PAGE_RANGE
+
+const char* device_bit_text(int bit) {
+  switch (bit) {
+    case PQKV_DEV_SLOT_RANGE: return "slot beyond the pool (token skipped)";
+    case PQKV_DEV_SEQ_RANGE: return "seq_len out of range (clamped)";
+    case PQKV_DEV_BAD_SCALE: return "scale not finite and positive";
+    case PQKV_DEV_TIMEOUT: return "pipeline wait timed out";
+    case PQKV_DEV_PAGE_RANGE: return "block-table page id out of range (read as zeros)";
+  }
+  return "";
+}
+
+// "device: a; b; ..." for every combination of the device status bits, built
+// once (a status word may hold several OR-ed bits).
+const std::string& device_bits_text(int bits) {
+  static const std::vector<std::string> table = [] {
+    std::vector<std::string> t(1u << kDevBits);
+    for (int c = 1; c < (1 << kDevBits); ++c) {
+      std::string s = "device: ";
+      bool first = true;
+      for (int b = 0; b < kDevBits; ++b) {
+        if (!(c & (1 << b))) continue;
+        if (!first) s += "; ";
+        s += device_bit_text(1 << b);
+        first = false;
+      }
+      t[c] = s;
+    }
+    return t;
+  }();
+  return table[bits];
+}
+
+}  // namespace
+}  // namespace pqkv
+
 extern "C" const char* pqkv_status_string(int code) {
   switch (code) {
     case PQKV_OK: return "ok";
@@ -393,12 +437,8 @@ extern "C" const char* pqkv_status_string(int code) {
     case PQKV_ERANGE: return "size outside the supported range";
     case PQKV_EWORKSPACE: return "workspace missing, misaligned or too small";
     case PQKV_ECUDA: return "CUDA runtime call or kernel launch failed";
-    case PQKV_DEV_SLOT_RANGE: return "device: slot beyond the pool (token skipped)";
-    case PQKV_DEV_SEQ_RANGE: return "device: seq_len out of range (clamped)";
-    case PQKV_DEV_BAD_SCALE: return "device: scale not finite and positive";
-    case PQKV_DEV_TIMEOUT: return "device: pipeline wait timed out";
-    case PQKV_DEV_PAGE_RANGE: return "device: block-table page id out of range (read as zeros)";
   }
+  if (code > 0 && code < (1 << pqkv::kDevBits)) return pqkv::device_bits_text(code).c_str();
   return "unknown status";
 }
 

@@ -3,10 +3,11 @@
 // cache holds E4M3 codes under calibrated per-layer scales, INT8 codes under a
 // per-head scale, or plain fp16.
 //
-// One thread owns one 16-element vector of one (token, kv-head) row for both K
-// and V: it reads 32 B of fp16 per tensor (two 16-byte loads), forms the
-// correctly rounded fp32 quotient x / scale for each element, converts with
-// round-to-nearest-even and saturation, and stores 16 codes (one 16-byte
+// One thread owns 16-element vectors of (token, kv-head) rows for both K and
+// V -- two per pass, whose loads are all issued before any arithmetic: per
+// vector it reads 32 B of fp16 per tensor (two 16-byte streaming loads), forms
+// the correctly rounded fp32 quotient x / scale for each element, converts
+// with round-to-nearest-even and saturation, and stores 16 codes (one 16-byte
 // store; 32 B for fp16).  Consecutive threads cover consecutive vectors of a
 // row, so loads are fully coalesced and each (token, head) row lands as one
 // 128-byte line of its page tile.
@@ -81,59 +82,83 @@ __device__ __forceinline__ uint4 quantize16(const uint4& a, const uint4& b, floa
 }
 
 template <int KVT>
-__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
   constexpr int kVecPerRow = kHeadDim / 16;
   constexpr int kElem = (KVT == PQKV_KV_FP16) ? 2 : 1;
   constexpr int64_t kTile = (int64_t)kPageSize * kHeadDim * kElem;  // one K (or V) tile
+  constexpr int U = kAppendUnroll;
   const int64_t total = (int64_t)p.num_tokens * p.num_kv_heads * kVecPerRow;
   const int64_t pool_slots = p.num_pages * kPageSize;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % kVecPerRow);
-    const int64_t th = i / kVecPerRow;
-    const int h = (int)(th % p.num_kv_heads);
-    const int64_t t = th / p.num_kv_heads;
-    const int64_t slot = p.slots[t];
-    if (slot < 0) continue;
-    if (slot >= pool_slots) {
-      if (c == 0 && h == 0) report(p.status, PQKV_DEV_SLOT_RANGE);
-      continue;
-    }
-    const int64_t page = slot / kPageSize;
-    const int off = (int)(slot % kPageSize);
-    const uint4* ks = reinterpret_cast<const uint4*>(p.k + t * p.k_stride + h * kHeadDim + c * 16);
-    const uint4* vs = reinterpret_cast<const uint4*>(p.v + t * p.v_stride + h * kHeadDim + c * 16);
-    const uint4 k0 = __ldg(ks), k1 = __ldg(ks + 1);
-    const uint4 v0 = __ldg(vs), v1 = __ldg(vs + 1);
-    uint8_t* tile = p.pages + (page * p.num_kv_heads + h) * 2 * kTile;
-    uint8_t* kd = tile + (int64_t)off * kHeadDim * kElem + c * 16 * kElem;
-    uint8_t* vd = kd + kTile;
-    if (KVT == PQKV_KV_FP16) {
-      reinterpret_cast<uint4*>(kd)[0] = k0;
-      reinterpret_cast<uint4*>(kd)[1] = k1;
-      reinterpret_cast<uint4*>(vd)[0] = v0;
-      reinterpret_cast<uint4*>(vd)[1] = v1;
-    } else if (KVT == PQKV_KV_INT8_ROW) {
-      // all eight threads of the row reach this point together
-      const float kscale = __fdiv_rn(row_max8(amax16(k0, k1)), 127.f);
-      const float vscale = __fdiv_rn(row_max8(amax16(v0, v1)), 127.f);
-      *reinterpret_cast<uint4*>(kd) = quantize16<PQKV_KV_INT8>(k0, k1, kscale);
-      *reinterpret_cast<uint4*>(vd) = quantize16<PQKV_KV_INT8>(v0, v1, vscale);
-      if (c == 0) {
-        float* rs = p.row_scales + (page * p.num_kv_heads + h) * 2 * kPageSize + off;
-        rs[0] = kscale;
-        rs[kPageSize] = vscale;
+  const int64_t stride = (int64_t)gridDim.x * kAppendThreads * U;
+  for (int64_t i0 = (int64_t)blockIdx.x * kAppendThreads * U + threadIdx.x; i0 < total;
+       i0 += stride) {
+    // ---- all loads of this pass first.  Vector u is i0 + u * blockDim; the
+    //      eight vectors of one (token, kv-head) row sit in eight consecutive
+    //      lanes, so a row is either wholly in range or wholly out.
+    int64_t slot[U], t[U];
+    int h[U], c[U];
+    uint4 k0[U], k1[U], v0[U], v1[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + (int64_t)u * kAppendThreads;
+      slot[u] = -1;
+      if (i < total) {
+        c[u] = (int)(i % kVecPerRow);
+        const int64_t th = i / kVecPerRow;
+        h[u] = (int)(th % p.num_kv_heads);
+        t[u] = th / p.num_kv_heads;
+        slot[u] = __ldg(p.slots + t[u]);
+        const uint4* ks = reinterpret_cast<const uint4*>(p.k + t[u] * p.k_stride +
+                                                         h[u] * kHeadDim + c[u] * 16);
+        const uint4* vs = reinterpret_cast<const uint4*>(p.v + t[u] * p.v_stride +
+                                                         h[u] * kHeadDim + c[u] * 16);
+        k0[u] = __ldcs(ks);
+        k1[u] = __ldcs(ks + 1);
+        v0[u] = __ldcs(vs);
+        v1[u] = __ldcs(vs + 1);
       }
-    } else {
-      const int sh = p.scale_per_head ? h : 0;
-      const float kscale = __ldg(p.k_scale + sh);
-      const float vscale = __ldg(p.v_scale + sh);
-      if (!scale_ok(kscale) || !scale_ok(vscale)) {
-        if (c == 0) report(p.status, PQKV_DEV_BAD_SCALE);
+    }
+    // ---- then convert and store
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + (int64_t)u * kAppendThreads;
+      if (i >= total || slot[u] < 0) continue;
+      if (slot[u] >= pool_slots) {
+        if (c[u] == 0 && h[u] == 0) report(p.status, PQKV_DEV_SLOT_RANGE);
         continue;
       }
-      *reinterpret_cast<uint4*>(kd) = quantize16<KVT>(k0, k1, kscale);
-      *reinterpret_cast<uint4*>(vd) = quantize16<KVT>(v0, v1, vscale);
+      const int64_t page = slot[u] / kPageSize;
+      const int off = (int)(slot[u] % kPageSize);
+      uint8_t* tile = p.pages + (page * p.num_kv_heads + h[u]) * 2 * kTile;
+      uint8_t* kd = tile + (int64_t)off * kHeadDim * kElem + c[u] * 16 * kElem;
+      uint8_t* vd = kd + kTile;
+      if (KVT == PQKV_KV_FP16) {
+        reinterpret_cast<uint4*>(kd)[0] = k0[u];
+        reinterpret_cast<uint4*>(kd)[1] = k1[u];
+        reinterpret_cast<uint4*>(vd)[0] = v0[u];
+        reinterpret_cast<uint4*>(vd)[1] = v1[u];
+      } else if (KVT == PQKV_KV_INT8_ROW) {
+        // all eight threads of the row reach this point together
+        const float kscale = __fdiv_rn(row_max8(amax16(k0[u], k1[u])), 127.f);
+        const float vscale = __fdiv_rn(row_max8(amax16(v0[u], v1[u])), 127.f);
+        *reinterpret_cast<uint4*>(kd) = quantize16<PQKV_KV_INT8>(k0[u], k1[u], kscale);
+        *reinterpret_cast<uint4*>(vd) = quantize16<PQKV_KV_INT8>(v0[u], v1[u], vscale);
+        if (c[u] == 0) {
+          float* rs = p.row_scales + (page * p.num_kv_heads + h[u]) * 2 * kPageSize + off;
+          rs[0] = kscale;
+          rs[kPageSize] = vscale;
+        }
+      } else {
+        const int sh = p.scale_per_head ? h[u] : 0;
+        const float kscale = __ldg(p.k_scale + sh);
+        const float vscale = __ldg(p.v_scale + sh);
+        if (!scale_ok(kscale) || !scale_ok(vscale)) {
+          if (c[u] == 0) report(p.status, PQKV_DEV_BAD_SCALE);
+          continue;
+        }
+        *reinterpret_cast<uint4*>(kd) = quantize16<KVT>(k0[u], k1[u], kscale);
+        *reinterpret_cast<uint4*>(vd) = quantize16<KVT>(v0[u], v1[u], vscale);
+      }
     }
   }
 }
@@ -141,16 +166,16 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream) {
   switch (kv_dtype) {
     case PQKV_KV_FP16:
-      append_kernel<PQKV_KV_FP16><<<grid, 256, 0, stream>>>(p);
+      append_kernel<PQKV_KV_FP16><<<grid, kAppendThreads, 0, stream>>>(p);
       break;
     case PQKV_KV_FP8_E4M3:
-      append_kernel<PQKV_KV_FP8_E4M3><<<grid, 256, 0, stream>>>(p);
+      append_kernel<PQKV_KV_FP8_E4M3><<<grid, kAppendThreads, 0, stream>>>(p);
       break;
     case PQKV_KV_INT8:
-      append_kernel<PQKV_KV_INT8><<<grid, 256, 0, stream>>>(p);
+      append_kernel<PQKV_KV_INT8><<<grid, kAppendThreads, 0, stream>>>(p);
       break;
     case PQKV_KV_INT8_ROW:
-      append_kernel<PQKV_KV_INT8_ROW><<<grid, 256, 0, stream>>>(p);
+      append_kernel<PQKV_KV_INT8_ROW><<<grid, kAppendThreads, 0, stream>>>(p);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -348,12 +348,17 @@ __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
 // ---------------------------------------------------------------------------
 template <class PP> struct IsPartial { static constexpr bool value = false; };
 template <> struct IsPartial<AttnPartialParams> { static constexpr bool value = true; };
+template <class PP> struct IsWaitTest { static constexpr bool value = false; };
+template <> struct IsWaitTest<AttnWaitTestParams> { static constexpr bool value = true; };
+constexpr uint64_t kTestWaitLimitNs = 1000000ull;   // 1 ms in the wait test
 
 template <int KVT, int NT, class PP = AttnParams>
 __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
     paged_attention_kernel(const __grid_constant__ CUtensorMap map, const PP p) {
   using Cfg = AttnCfg<KVT, NT>;
   constexpr bool kPartial = IsPartial<PP>::value;
+  constexpr bool kWaitTest = IsWaitTest<PP>::value;
+  constexpr uint64_t kLimitNs = kWaitTest ? kTestWaitLimitNs : kWaitLimitNs;
   constexpr int W = Cfg::kW, S = Cfg::kStages, SPW = Cfg::kStagesPerWarp, RP = Cfg::kRP;
   constexpr int nthr = W * 32;
   extern __shared__ uint8_t smem_raw[];
@@ -479,6 +484,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   lookup(lane, cur_id, cur_h);
   lookup(32 + lane, nxt_id, nxt_h);
   int issued_u = 0;                      // pages of this warp issued so far
+  int skipped_u = -1;                    // wait test: the page whose copy was never issued
   auto issue_next = [&]() {
     const int u = issued_u;
     const int i = warp + u * W;
@@ -491,6 +497,13 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
     }
     const int id = __shfl_sync(0xffffffffu, cur_id, u - ubase);
     const int h = __shfl_sync(0xffffffffu, cur_h, u - ubase);
+    if constexpr (kWaitTest) {
+      if ((int)blockIdx.x == p.skip_block && i == p.skip_page) {
+        skipped_u = u;
+        issued_u = u + 1;
+        return;
+      }
+    }
     if (lane == 0) {
       const int stage = i % S;
       if constexpr (Cfg::kRowScaled) {
@@ -617,7 +630,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         // one try first: the tile is usually there, and the abort flag (a
         // shared-memory read) only matters once some wait has run out
         bool ok = mbar_try_wait(&full[stage], (gi / S) & 1) ||
-                  (!*abort_flag && mbar_wait(&full[stage], (gi / S) & 1));
+                  (!*abort_flag && mbar_wait<kLimitNs>(&full[stage], (gi / S) & 1));
         ok = __all_sync(0xffffffffu, ok);       // keep the warp's control flow uniform
         if (!ok) {
           dead = true;
@@ -918,8 +931,9 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   //      can this warp have issued pages it did not consume)
   if (lane == 0 && *abort_flag) {
     for (int u = consumed_u; u < issued_u; ++u) {
+      if (kWaitTest && u == skipped_u) continue;     // nothing in flight there
       const int i = warp + u * W;
-      (void)mbar_wait(&full[i % S], (i / S) & 1);
+      (void)mbar_wait<kLimitNs>(&full[i % S], (i / S) & 1);
     }
   }
 }

@@ -9,7 +9,8 @@
 // owns: a fixed-size file-scope device array that every GPU that loads the
 // library holds until the process exits.  It allocates nothing and calls no
 // allocating routine; it is otherwise the same computation as
-// pqkv_paged_attention, which it calls with the scratch area as workspace.
+// pqkv_paged_attention, planned and launched by the same internal steps with
+// the scratch area as workspace.
 #include <cstring>
 #include <mutex>
 
@@ -51,23 +52,36 @@ extern "C" int pqkv_paged_attention_noalloc(const void* q, void* out, const void
                                             const float* k_scale, const float* v_scale,
                                             int32_t scale_per_head, int32_t num_splits,
                                             int32_t max_seq_len, int32_t* status, void* stream) {
-  if (num_splits < 0 || num_splits > PQKV_MAX_SPLITS) return PQKV_ERANGE;
-  const size_t need = pqkv_paged_attention_workspace_size(num_seqs, q_len, num_q_heads,
-                                                          num_kv_heads, head_dim, num_splits);
-  if (need > PQKV_NOALLOC_SCRATCH_BYTES) return PQKV_ERANGE;
+  using namespace pqkv;
+  const AttnArgs a{q, pages, num_pages, block_table, max_pages_per_seq, seq_lens, num_seqs, q_len,
+                   num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype, k_scale, v_scale,
+                   scale_per_head, num_splits, max_seq_len};
+  int rc = check_output_args(a, !out || (reinterpret_cast<uintptr_t>(out) % 16) != 0);
+  if (rc) return rc;
+  // Every check runs before anything is queued on the stream: a call that is
+  // rejected leaves the shared scratch area alone.
+  AttnLaunch L;
+  rc = plan_attention_launch(a, &L);
+  if (rc || num_seqs == 0) return rc;
+  // the workspace of the grid this call launches (not the largest grid)
+  if (L.pl.total > PQKV_NOALLOC_SCRATCH_BYTES) return PQKV_ERANGE;
   void* scratch = nullptr;
-  if (need > 0) {
-    const int rc = scratch_address(&scratch);
+  if (L.pl.total > 0) {
+    rc = scratch_address(&scratch);
     if (rc) return rc;
+  }
+  AttnParams p;
+  CUtensorMap map;
+  rc = bind_attention(a, L, scratch, L.pl.total > 0 ? (size_t)PQKV_NOALLOC_SCRATCH_BYTES : 0,
+                      status, &p, &map);
+  if (rc) return rc;
+  p.out = static_cast<uint16_t*>(out);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (L.pl.total > 0) {
     // The array keeps the previous call's contents; the merge counters at its
     // start must be zero when the kernel begins.
-    const size_t counters = PQKV_COUNTER_BYTES(num_seqs, num_kv_heads);
-    if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return PQKV_ECUDA;
+    if (cudaMemsetAsync(scratch, 0, L.pl.counter_bytes, st) != cudaSuccess) return PQKV_ECUDA;
   }
-  return pqkv_paged_attention(q, out, pages, num_pages, block_table, max_pages_per_seq, seq_lens,
-                              num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
-                              kv_dtype, k_scale, v_scale, scale_per_head, num_splits, max_seq_len,
-                              scratch, need > 0 ? (size_t)PQKV_NOALLOC_SCRATCH_BYTES : 0, status,
-                              stream);
+  return launch_attention(kv_dtype, p, map, L.grid, L.nt, st) == cudaSuccess ? PQKV_OK
+                                                                              : PQKV_ECUDA;
 }

@@ -64,16 +64,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Wait until the phase of the given parity has completed.  Gives up after
-// kWaitLimitNs of wall time and returns false; the caller reports
-// PQKV_DEV_TIMEOUT and stops.
+// kLimitNs of wall time (1 s unless a test instantiation lowers it) and
+// returns false; the caller reports PQKV_DEV_TIMEOUT and stops.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
+template <uint64_t kLimitNs = kWaitLimitNs>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((n & 255u) == 0 && globaltimer_ns() - t0 > kLimitNs) return false;
   }
 }
 

@@ -65,6 +65,16 @@ struct AttnPartialParams : AttnParams {
   float* out_lse;           // [B*q_len][Hq]
 };
 
+// Test mode of the bounded waits: the feed of block `skip_block` does not
+// issue the copy of that block's page `skip_page` (its position in the
+// block's share), so the warp that owns the page waits for a tile that never
+// comes; waits give up after 1 ms instead of 1 s.  Built only into the
+// testing entry point.
+struct AttnWaitTestParams : AttnParams {
+  int32_t skip_block;
+  int32_t skip_page;
+};
+
 // Host launchers (one per KV format), defined in the attention translation units.
 cudaError_t launch_attention_fp16(const AttnParams& p, const CUtensorMap& map, int grid,
                                   int nt, cudaStream_t stream);
@@ -89,10 +99,59 @@ cudaError_t launch_attention_partial_int8(const AttnPartialParams& p, const CUte
                                           int grid, int nt, cudaStream_t stream);
 cudaError_t launch_attention_partial_int8_row(const AttnPartialParams& p, const CUtensorMap& map,
                                               int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_wait_test_e4m3(const AttnWaitTestParams& p, const CUtensorMap& map,
+                                            int grid, int nt, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int num_parts,
                              int64_t rows, uint16_t* out, float* out_lse, cudaStream_t stream);
 
+// Append launch shape: blocks of kAppendThreads threads, each thread takes
+// kAppendUnroll 16-element vectors per pass with every load of the pass
+// issued before the first division (kAppendUnroll * 64 bytes in flight).
+constexpr int kAppendThreads = 256;
+constexpr int kAppendUnroll = 2;
 cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream);
+
+// The arguments of one attention call (the shared part of the entry points).
+struct AttnArgs {
+  const void* q;
+  const void* pages;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int32_t max_pages_per_seq;
+  const int32_t* seq_lens;
+  int32_t num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t scale_per_head, num_splits, max_seq_len;
+};
+
+// Workspace carve-up of one call: merge counters, partial O, partial (m, l).
+struct AttnPlan {
+  int rows = 0, rp = 0, nt = 0;
+  int64_t slots = 0;        // partial-result slots
+  size_t counter_bytes = 0, o_bytes = 0, ml_bytes = 0, total = 0;
+};
+
+// Launch shape of one validated call: grid, row tiles and the workspace it needs.
+struct AttnLaunch {
+  int grid = 0, nt = 0, rows = 0;
+  AttnPlan pl;
+};
+
+// Validate the arguments and size the launch (grid and workspace need) on the
+// current device.  Queues nothing.  num_seqs == 0 returns PQKV_OK with an
+// empty launch.
+int plan_attention_launch(const AttnArgs& a, AttnLaunch* L);
+// Check the workspace against the launch, encode the pool's TMA map and fill
+// the kernel parameters (all but the outputs).  Queues nothing.
+int bind_attention(const AttnArgs& a, const AttnLaunch& L, void* workspace,
+                   size_t workspace_bytes, int32_t* status, AttnParams* p, CUtensorMap* map);
+// Launch the attention kernel of the pool's format.
+cudaError_t launch_attention(int kv_dtype, const AttnParams& p, const CUtensorMap& map, int grid,
+                             int nt, cudaStream_t stream);
+// PQKV_EINVAL (after the size checks) when num_seqs > 0 and an output
+// argument is missing or misaligned.
+int check_output_args(const AttnArgs& a, bool bad_outputs);
 
 inline int rows_padded(int rows) { return ((rows + 7) / 8) * 8; }
 

@@ -51,6 +51,22 @@ def test_version_and_status_strings(lib):
     for code in [OK, EINVAL, EUNSUPPORTED, ERANGE, EWORKSPACE, ECUDA, 1, 2, 4, 8, 16]:
         assert lib.pqkv_status_string(code) not in (None, b"unknown status")
     assert lib.pqkv_status_string(12345) == b"unknown status"
+    assert lib.pqkv_status_string(32) == b"unknown status"
+
+
+def test_status_string_names_every_bit_of_a_combined_word(lib):
+    single = {b: lib.pqkv_status_string(b).decode() for b in (1, 2, 4, 8, 16)}
+    for b, text in single.items():
+        assert text.startswith("device: ")
+    for word in range(1, 32):
+        text = lib.pqkv_status_string(word).decode()
+        assert text.startswith("device: ")
+        parts = text[len("device: "):].split("; ")
+        want = [single[b][len("device: "):] for b in (1, 2, 4, 8, 16) if word & b]
+        assert parts == want, (word, text)
+    # PQKV_DEV_SLOT_RANGE | PQKV_DEV_BAD_SCALE
+    assert lib.pqkv_status_string(5) == (b"device: slot beyond the pool (token skipped); "
+                                         b"scale not finite and positive")
 
 
 def _append(lib, **kw):

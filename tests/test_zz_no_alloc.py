@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from tests.helpers import Case, assert_close, require_gpu
 
@@ -68,3 +69,44 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     one = torch.ones(1, dtype=torch.float32, device="cuda")
     with pytest.raises(ValueError):
         pq.paged_attention_noalloc(q, pages, bt, sl, q_len, W.FP8_E4M3, one, one, torch.empty_like(q))
+
+
+def test_noalloc_32_row_verify_against_the_oracle():
+    """q_len 8 with 4 query heads per kv-head: 32 rows, the widest row tile.
+    The scratch it needs is sized from the grid the call launches, so the
+    default balanced split fits whatever the context length."""
+    pq = require_gpu()
+    c = Case(W.workload("e4m3_verify_q8_131k", scale=0.004), with_oracle=True)
+    ref = c.oracle_attention()
+    for call in range(2):
+        out = torch.full_like(c.q, float("nan"))
+        _noalloc(pq, c, out, 0)
+        torch.cuda.synchronize()
+        assert_close(out, ref, "noalloc 32 rows call %d" % call)
+
+
+def test_noalloc_largest_fixed_split_that_fits():
+    """The stress verify (8 sequences x 8 kv-heads, 24 padded rows) cut into
+    21 fixed partitions per (sequence, kv-head) needs 16,773,376 bytes of
+    scratch, just under the 16 MiB area; two calls in a row must both match
+    the oracle (the merge counters are cleared between calls).  22 partitions
+    no longer fit and are refused before anything is queued."""
+    pq = require_gpu()
+    c = Case(W.workload("e4m3_verify_512k_stress", scale=0.004), with_oracle=True)
+    assert pq.workspace_size(8, 5, 32, 8, 21) == 16773376 <= pq.NOALLOC_SCRATCH_BYTES
+    assert pq.workspace_size(8, 5, 32, 8, 22) > pq.NOALLOC_SCRATCH_BYTES
+    ref = c.oracle_attention()
+    for call in range(2):
+        out = torch.full_like(c.q, float("nan"))
+        _noalloc(pq, c, out, 21)
+        torch.cuda.synchronize()
+        assert_close(out, ref, "noalloc 21 splits call %d" % call)
+    before = out.clone()
+    with pytest.raises(ValueError):
+        _noalloc(pq, c, out, 22)
+    torch.cuda.synchronize()
+    assert torch.equal(out, before)
+    # a valid call after the refused one is still right
+    out2 = torch.empty_like(c.q)
+    _noalloc(pq, c, out2, 21)
+    assert_close(out2, ref, "noalloc after a refused call")
