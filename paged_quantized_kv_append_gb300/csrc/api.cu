@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxGrid = 1024;           // upper bound of the balanced grid
-constexpr int kMinPagesPerBlock = 16;    // smallest balanced share worth a block
+constexpr int kMinPagesPerBlock = 8;     // smallest balanced share worth a block
 
 struct DeviceInfo {
   bool ready = false;
