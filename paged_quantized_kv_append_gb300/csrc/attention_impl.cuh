@@ -65,13 +65,19 @@ struct AttnCfg {
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kRingOff = 0;
   static constexpr int kOOff = kRingOff + kStages * kTileBytes;
-  // With 12 or 16 warps the warps' O are combined in groups of four (warp w
-  // into buffer w / 4, in turn inside the group), then the group buffers are
-  // added in fixed order; 8 warps take turns on one buffer.
+  // Fragment-end combine of the warps' O.  8 and 16 query rows: a tree (in
+  // each round the upper half of the remaining warps hands its O to the lower
+  // half, kW / 2 buffers in the first round; warp 0 writes the result from
+  // registers).  24 and 32 rows: groups of four warps take turns on a group
+  // buffer (8 warps: one group), then the group buffers are added in fixed
+  // order -- the 24-row page loop compiled slower with the tree epilogue,
+  // and the 32-row kernel has no shared memory left for its buffers.
+  static constexpr bool kTree = NT <= 2;
   static constexpr int kCombGroups = kW >= 12 ? kW / 4 : 1;
   static constexpr int kCombSize = kW / kCombGroups;
-  static constexpr int kOBytes = kRP * kHeadDim * 4;     // one group buffer
-  static constexpr int kMLOff = kOOff + kCombGroups * kOBytes;
+  static constexpr int kOBytes = kRP * kHeadDim * 4;     // one buffer
+  static constexpr int kOBuffers = kTree ? kW / 2 : kCombGroups;
+  static constexpr int kMLOff = kOOff + kOBuffers * kOBytes;
   static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
   static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
   // INT8_ROW: the 32 row scales (16 K, 16 V) of each stage's (page, kv-head)
@@ -286,10 +292,10 @@ struct VMask {
 // dims 16g + 2mt (A rows g) and 16g + 2mt + 1 (A rows g + 8) of tokens
 // (2t, 2t+1) and (2t+8, 2t+9).  When `masked`, tokens past the sequence end
 // are zeroed: their probability is 0, but a stale NaN code times 0 is NaN.
-template <int KVT, int NT>
+template <int KVT, int NT, class AfterLoads>
 __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
                                         const uint32_t (&pb)[NT][2], bool masked, const VMask& vm,
-                                        float (&o)[8][NT][4]) {
+                                        float (&o)[8][NT][4], AfterLoads after_loads) {
   auto mma_mt = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
     if (masked) {
       a0 &= vm.m01;
@@ -320,6 +326,7 @@ __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
     const uint4 C = lds128(T, 24 + 2 * t, g), D = lds128(T, 25 + 2 * t, g);
     const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w};
     const uint32_t c[4] = {C.x, C.y, C.z, C.w}, d[4] = {D.x, D.y, D.z, D.w};
+    after_loads();
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       if (KVT == PQKV_KV_FP8_E4M3) {
@@ -374,6 +381,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   volatile int* abort_flag = misc + 0;
   volatile int* merge_flag = misc + 1;
   volatile int* has_frag = misc + 2;
+  volatile int* frag_cnt = misc + 3;
   float* sWarp = reinterpret_cast<float*>(misc + 16);          // [W] per-warp scratch
   float* sMrow = sWarp + W;                                    // [RP]
   float* sLrow = sMrow + RP;                                   // [RP]
@@ -741,16 +749,30 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         const bool tail = pos0 + kPageSize > cur_L;
         VMask vm;
         vm.init(t, cur_L - pos0);
-        page_pv<KVT, NT>(T, g, t, pb, tail, vm, o);
+        if constexpr (Cfg::kRowScaled) {
+          // the stage is free once its V codes are in registers: refill it
+          // with this warp's page S ahead before the PV products
+          page_pv<KVT, NT>(T, g, t, pb, tail, vm, o, [&]() {
+            __syncwarp();
+            fence_proxy_async_smem();
+            consumed_u += 1;
+            issue_next();
+          });
+        } else {
+          page_pv<KVT, NT>(T, g, t, pb, tail, vm, o, []() {});
+        }
       }
-      // the stage is free again: refill it with this warp's page S ahead
-      __syncwarp();
-      fence_proxy_async_smem();
-      consumed_u += 1;
-      issue_next();
+      if constexpr (!Cfg::kRowScaled) {
+        // the stage is free again: refill it with this warp's page S ahead
+        __syncwarp();
+        fence_proxy_async_smem();
+        consumed_u += 1;
+        issue_next();
+      }
     }
     n0 += npg;
 
+    if constexpr (!Cfg::kTree) {
     // ---- combine the warps' states of this fragment: every warp publishes
     // its (m, l) per row, then the warps add their rescaled O into their
     // group's shared buffer, the members of a group in turn (all groups at
@@ -923,6 +945,219 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
         }
         if (tid == 0) p.counters[f_seg] = 0;
       }
+    }
+    } else {
+    // ---- fragment end.  Every warp publishes its (m, l) per row; each warp
+    // rescales its O to the block's row maximum; a tree then adds the warps'
+    // O (in each round the upper half of the remaining warps hands its O to
+    // the lower half through shared memory), so warp 0 ends with the
+    // fragment's O in registers and writes the output or the partial from
+    // there.  Fixed order throughout, so the result is deterministic.
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float l = lsum[nt][c];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (g == 0) {
+          const int r = 8 * nt + 2 * t + c;
+          sML[(warp * 2 + 0) * RP + r] = mref[nt][c];
+          sML[(warp * 2 + 1) * RP + r] = l;
+        }
+      }
+    if (tid == 0) *frag_cnt = sp.count(f_seg, sf->a, sf->b);
+    __syncthreads();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int r = 8 * nt + 2 * t + c;
+        float M = sML[r];
+#pragma unroll
+        for (int w = 1; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
+        const float fw = ex2(mref[nt][c] - M);
+        mref[nt][c] = M;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][nt][c] *= fw;
+          o[mt][nt][c + 2] *= fw;
+        }
+      }
+#pragma unroll 1
+    for (int n = W; n > 1;) {
+      const int half = (n + 1) >> 1;
+      if (warp >= half && warp < n) {
+        float4* dst = reinterpret_cast<float4*>(sO + (size_t)(warp - half) * RP * kHeadDim);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              dst[((8 * nt + 2 * t + c) * kHeadDim + 16 * g) / 4 + k4] =
+                  make_float4(o[2 * k4][nt][c], o[2 * k4][nt][c + 2], o[2 * k4 + 1][nt][c],
+                              o[2 * k4 + 1][nt][c + 2]);
+      }
+      __syncthreads();
+      if (warp < n - half) {
+        const float4* src = reinterpret_cast<const float4*>(sO + (size_t)warp * RP * kHeadDim);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const float4 v = src[((8 * nt + 2 * t + c) * kHeadDim + 16 * g) / 4 + k4];
+              o[2 * k4][nt][c] += v.x;
+              o[2 * k4][nt][c + 2] += v.y;
+              o[2 * k4 + 1][nt][c] += v.z;
+              o[2 * k4 + 1][nt][c + 2] += v.w;
+            }
+      }
+      __syncthreads();
+      n = half;
+    }
+
+    const int cnt = *frag_cnt;
+    const int slot = sp.k > 0 ? (int)blockIdx.x : f_seg + (int)blockIdx.x;
+    const int64_t out_row0 = (int64_t)f_s * p.q_len;
+    if (warp == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int r = 8 * nt + 2 * t + c;
+          if (r >= p.rows) continue;
+          const float M = mref[nt][c];
+          float l = 0.f;
+#pragma unroll
+          for (int w = 0; w < W; ++w) l += ex2(sML[(w * 2) * RP + r] - M) * sML[(w * 2 + 1) * RP + r];
+          const int i = r / p.group, gh = r % p.group;
+          const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+          if (cnt == 1) {
+            const float f = l > 0.f ? v_mult / l : 0.f;
+            if constexpr (kPartial) {
+              float4* dst = reinterpret_cast<float4*>(p.out_o + orow * kHeadDim + 16 * g);
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4)
+                dst[k4] = make_float4(o[2 * k4][nt][c] * f, o[2 * k4][nt][c + 2] * f,
+                                      o[2 * k4 + 1][nt][c] * f, o[2 * k4 + 1][nt][c + 2] * f);
+              if (g == 0) p.out_lse[orow] = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
+            } else {
+              uint32_t hv[8];
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt)
+                hv[mt] = pack_half2(o[mt][nt][c] * f, o[mt][nt][c + 2] * f);
+              uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 16 * g);
+              dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+              dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)slot * RP + r) * kHeadDim +
+                                                    16 * g);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              dst[k4] = make_float4(o[2 * k4][nt][c], o[2 * k4][nt][c + 2], o[2 * k4 + 1][nt][c],
+                                    o[2 * k4 + 1][nt][c + 2]);
+            if (g == 0) {
+              p.part_ml[(size_t)slot * 2 * RP + r] = M;
+              p.part_ml[(size_t)slot * 2 * RP + RP + r] = l;
+            }
+          }
+        }
+    }
+        if (cnt > 1) {
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int ticket = atomicAdd(p.counters + f_seg, 1);
+        *merge_flag = (ticket == cnt - 1);
+      }
+      __syncthreads();
+      if (*merge_flag) {
+        __threadfence();
+        // gather the segment's partial slots (fixed order) into shared memory
+        int* slots = reinterpret_cast<int*>(sO);
+        if (tid == 0) {
+          int nsl = 0;
+          if (sp.k > 0) {
+            const int np = sp.pages(f_s);
+            for (int q = 0; q < sp.k; ++q)
+              if ((int64_t)(q + 1) * np / sp.k > (int64_t)q * np / sp.k)
+                slots[nsl++] = f_seg * sp.k + q;
+          } else {
+            for (int64_t x = sf->a; x < sf->b;) {
+              const int cc = sp.cta_of(x);
+              slots[nsl++] = f_seg + cc;
+              x = sp.start(cc + 1);
+            }
+          }
+        }
+        __syncthreads();
+        // per-row maximum and normaliser: the (m, l) of eight partials are
+        // loaded at once and folded in with a running rescale
+        if (tid < p.rows) {
+          const int r = tid;
+          float M = kNoScore, l = 0.f;
+          for (int q0 = 0; q0 < cnt; q0 += 8) {
+            float mq[8], lq[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const bool in = q0 + k < cnt;
+              const float* ml = p.part_ml + (size_t)slots[in ? q0 + k : 0] * 2 * RP;
+              mq[k] = in ? __ldcg(ml + r) : kNoScore;
+              lq[k] = in ? __ldcg(ml + RP + r) : 0.f;
+            }
+            float Mn = M;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mq[k]);
+            l *= ex2(M - Mn);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) l += ex2(mq[k] - Mn) * lq[k];
+            M = Mn;
+          }
+          sMrow[r] = M;
+          sLrow[r] = l;
+        }
+        __syncthreads();
+                const int dq = lane, rg = warp;
+        for (int r = rg; r < p.rows; r += W) {
+          const float M = sMrow[r];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+          for (int q = 0; q < cnt; ++q) {
+            const size_t sl = slots[q];
+            const float wq = ex2(__ldcg(p.part_ml + sl * 2 * RP + r) - M);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                        p.part_o + (sl * RP + r) * kHeadDim) +
+                                    dq);
+            acc.x += wq * v.x;
+            acc.y += wq * v.y;
+            acc.z += wq * v.z;
+            acc.w += wq * v.w;
+          }
+          const float inv = sLrow[r] > 0.f ? v_mult / sLrow[r] : 0.f;
+          const int i = r / p.group, gh = r % p.group;
+          const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+          if constexpr (kPartial) {
+            *reinterpret_cast<float4*>(p.out_o + orow * kHeadDim + 4 * dq) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (dq == 0)
+              p.out_lse[orow] = sLrow[r] > 0.f ? (M + __log2f(sLrow[r])) * kLn2 : -INFINITY;
+          } else {
+            __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
+            __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+          }
+        }
+        if (tid == 0) p.counters[f_seg] = 0;
+      }
+    }
     }
     __syncthreads();
   }
