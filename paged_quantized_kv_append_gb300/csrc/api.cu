@@ -19,6 +19,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxGrid = 1024;           // upper bound of the balanced grid
 constexpr int kMinPagesPerBlock = 8;     // smallest balanced share worth a block
+// 8-row decodes of 8-bit pools with at most this many (page, kv-head) units
+// per SM run as two 8-warp blocks per SM (one 16-warp block otherwise):
+// short contexts gain from the two blocks' unsynchronised start-up and
+// fragment ends, long ones stream faster with one block.
+constexpr int64_t kPairMaxUnitsPerSm = 1024;
 
 struct DeviceInfo {
   bool ready = false;
@@ -72,12 +77,12 @@ float* row_scale_area(void* pages, int64_t num_pages, int32_t num_kv_heads) {
                                   num_pages * num_kv_heads * 2 * kPageSize * kHeadDim);
 }
 
-int blocks_per_sm(int kv_dtype, int nt, int num_seqs) {
+int blocks_per_sm(int kv_dtype, int nt, bool pair, int num_seqs) {
   switch (kv_dtype) {
-    case PQKV_KV_FP16: return attention_blocks_per_sm_fp16(nt, num_seqs);
-    case PQKV_KV_FP8_E4M3: return attention_blocks_per_sm_e4m3(nt, num_seqs);
-    case PQKV_KV_INT8: return attention_blocks_per_sm_int8(nt, num_seqs);
-    case PQKV_KV_INT8_ROW: return attention_blocks_per_sm_int8_row(nt, num_seqs);
+    case PQKV_KV_FP16: return attention_blocks_per_sm_fp16(nt, pair, num_seqs);
+    case PQKV_KV_FP8_E4M3: return attention_blocks_per_sm_e4m3(nt, pair, num_seqs);
+    case PQKV_KV_INT8: return attention_blocks_per_sm_int8(nt, pair, num_seqs);
+    case PQKV_KV_INT8_ROW: return attention_blocks_per_sm_int8_row(nt, pair, num_seqs);
   }
   return 0;
 }
@@ -210,13 +215,15 @@ int plan_attention_launch(const AttnArgs& a, AttnLaunch* L) {
 
   // grid
   int grid;
+  bool pair = false;
   if (a.num_splits == 0) {
-    const int per_sm = blocks_per_sm(a.kv_dtype, nt, a.num_seqs);
-    if (per_sm <= 0) return PQKV_ECUDA;
     const int64_t cap_len = (int64_t)a.max_pages_per_seq * a.page_size;
     const int64_t lmax = a.max_seq_len > 0 ? std::min<int64_t>(a.max_seq_len, cap_len) : cap_len;
     const int64_t units =
         (int64_t)a.num_seqs * a.num_kv_heads * ((lmax + a.page_size - 1) / a.page_size);
+    pair = nt == 1 && a.kv_dtype != PQKV_KV_FP16 && units <= kPairMaxUnitsPerSm * sms;
+    const int per_sm = blocks_per_sm(a.kv_dtype, nt, pair, a.num_seqs);
+    if (per_sm <= 0) return PQKV_ECUDA;
     const int64_t want = (units + kMinPagesPerBlock - 1) / kMinPagesPerBlock;
     const int64_t cap = std::min<int64_t>((int64_t)sms * per_sm, (int64_t)kMaxGrid);
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, cap));
@@ -228,6 +235,7 @@ int plan_attention_launch(const AttnArgs& a, AttnLaunch* L) {
   plan_attention(a.num_seqs, a.q_len, a.num_q_heads, a.num_kv_heads, a.num_splits, grid, &L->pl);
   L->grid = grid;
   L->nt = nt;
+  L->pair = pair;
   L->rows = rows;
   return PQKV_OK;
 }
@@ -291,12 +299,12 @@ int bind_attention(const AttnArgs& a, const AttnLaunch& L, void* workspace,
 }
 
 cudaError_t launch_attention(int kv_dtype, const AttnParams& p, const CUtensorMap& map, int grid,
-                             int nt, cudaStream_t st) {
+                             int nt, bool pair, cudaStream_t st) {
   switch (kv_dtype) {
-    case PQKV_KV_FP16: return launch_attention_fp16(p, map, grid, nt, st);
-    case PQKV_KV_FP8_E4M3: return launch_attention_e4m3(p, map, grid, nt, st);
-    case PQKV_KV_INT8_ROW: return launch_attention_int8_row(p, map, grid, nt, st);
-    default: return launch_attention_int8(p, map, grid, nt, st);
+    case PQKV_KV_FP16: return launch_attention_fp16(p, map, grid, nt, pair, st);
+    case PQKV_KV_FP8_E4M3: return launch_attention_e4m3(p, map, grid, nt, pair, st);
+    case PQKV_KV_INT8_ROW: return launch_attention_int8_row(p, map, grid, nt, pair, st);
+    default: return launch_attention_int8(p, map, grid, nt, pair, st);
   }
 }
 
@@ -335,7 +343,7 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   if (rc) return rc;
   p.out = static_cast<uint16_t*>(out);
   const cudaError_t e =
-      launch_attention(kv_dtype, p, map, L.grid, L.nt, static_cast<cudaStream_t>(stream));
+      launch_attention(kv_dtype, p, map, L.grid, L.nt, L.pair, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }
 
@@ -365,10 +373,10 @@ extern "C" int pqkv_paged_attention_partial(
   cudaError_t e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (kv_dtype) {
-    case PQKV_KV_FP16: e = launch_attention_partial_fp16(p, map, L.grid, L.nt, st); break;
-    case PQKV_KV_FP8_E4M3: e = launch_attention_partial_e4m3(p, map, L.grid, L.nt, st); break;
-    case PQKV_KV_INT8_ROW: e = launch_attention_partial_int8_row(p, map, L.grid, L.nt, st); break;
-    default: e = launch_attention_partial_int8(p, map, L.grid, L.nt, st); break;
+    case PQKV_KV_FP16: e = launch_attention_partial_fp16(p, map, L.grid, L.nt, L.pair, st); break;
+    case PQKV_KV_FP8_E4M3: e = launch_attention_partial_e4m3(p, map, L.grid, L.nt, L.pair, st); break;
+    case PQKV_KV_INT8_ROW: e = launch_attention_partial_int8_row(p, map, L.grid, L.nt, L.pair, st); break;
+    default: e = launch_attention_partial_int8(p, map, L.grid, L.nt, L.pair, st); break;
   }
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }

@@ -4,18 +4,18 @@
 
 namespace pqkv {
 
-cudaError_t launch_attention_fp16(const AttnParams& p, const CUtensorMap& map, int grid, int nt,
-                                  cudaStream_t stream) {
-  return launch_attention_dtype<PQKV_KV_FP16>(p, map, grid, nt, stream);
+cudaError_t launch_attention_fp16(const AttnParams& p, const CUtensorMap& map, int grid,
+                                  int nt, bool pair, cudaStream_t stream) {
+  return launch_attention_dtype<PQKV_KV_FP16>(p, map, grid, nt, pair, stream);
 }
 
-int attention_blocks_per_sm_fp16(int nt, int num_seqs) {
-  return blocks_per_sm_dtype<PQKV_KV_FP16>(nt, num_seqs);
+int attention_blocks_per_sm_fp16(int nt, bool pair, int num_seqs) {
+  return blocks_per_sm_dtype<PQKV_KV_FP16>(nt, pair, num_seqs);
 }
 
 cudaError_t launch_attention_partial_fp16(const AttnPartialParams& p, const CUtensorMap& map,
-                                          int grid, int nt, cudaStream_t stream) {
-  return launch_attention_partial_dtype<PQKV_KV_FP16>(p, map, grid, nt, stream);
+                                          int grid, int nt, bool pair, cudaStream_t stream) {
+  return launch_attention_partial_dtype<PQKV_KV_FP16>(p, map, grid, nt, pair, stream);
 }
 
 }  // namespace pqkv

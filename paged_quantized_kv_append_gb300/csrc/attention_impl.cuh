@@ -42,7 +42,7 @@
 
 namespace pqkv {
 
-template <int KVT, int NT>
+template <int KVT, int NT, bool kPair = false>
 struct AttnCfg {
   // One block per SM.  Every warp is a consumer and feeds its own slice of the
   // TMA ring: page i of the block goes to warp i % kW and stage i % kStages,
@@ -53,12 +53,19 @@ struct AttnCfg {
   // multiples of 4, because registers are allotted per scheduler (a quarter
   // of the SM): 8 warps get 255 registers each, 12 get 168, 16 get 128.
   // 8 query rows (NT 1) run 16 warps, 16 rows 12, and 24 or 32 rows 8.
-  static constexpr int kW = (KVT == PQKV_KV_FP16) ? 8 : (NT == 1 ? 16 : (NT == 2 ? 12 : 8));
+  static constexpr int kW =
+      (KVT == PQKV_KV_FP16 || kPair) ? 8 : (NT == 1 ? 16 : (NT == 2 ? 12 : 8));
+  // kPair (8 query rows, 8-bit codes, short contexts): two 8-warp blocks per
+  // SM at 128 registers, each with half the ring, instead of one 16-warp
+  // block; the two blocks' start-up and fragment ends do not wait on each
+  // other.
+  static constexpr int kMinBlocks = kPair ? 2 : 1;
+  static_assert(!kPair || (NT == 1 && KVT != PQKV_KV_FP16), "paired blocks: 8-row 8-bit decode only");
   static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
   static constexpr int kTileBytes = kLines * 128;
   static constexpr int kStagesPerWarp =
-      (KVT == PQKV_KV_FP16) ? 2 : (kW <= 8 ? 4 : (kW == 12 ? 3 : 2));
+      (KVT == PQKV_KV_FP16 || kPair) ? 2 : (kW <= 8 ? 4 : (kW == 12 ? 3 : 2));
   static constexpr int kStages = kW * kStagesPerWarp;
   static constexpr int kRP = 8 * NT;                               // padded query rows
   static constexpr int kQfBytes = 8 * NT * 32 * 8;
@@ -137,6 +144,21 @@ struct Split {
     int n = 0;
     for (int64_t x = a; x < b; x = start(cta_of(x) + 1)) ++n;
     return n;
+  }
+
+  // The same in constant time when every block's share is non-empty (P >= C):
+  // the blocks holding units of [a, b) are then exactly first .. first + n - 1.
+  __device__ __forceinline__ int count_fast(int seg, int64_t a, int64_t b, int& first) const {
+    if (k > 0) {
+      first = 0;
+      return min(k, pages(seg / H));
+    }
+    if (P < C) {
+      first = -1;
+      return count(seg, a, b);
+    }
+    first = cta_of(a);
+    return cta_of(b - 1) - first + 1;
   }
 };
 
@@ -359,10 +381,11 @@ template <class PP> struct IsWaitTest { static constexpr bool value = false; };
 template <> struct IsWaitTest<AttnWaitTestParams> { static constexpr bool value = true; };
 constexpr uint64_t kTestWaitLimitNs = 1000000ull;   // 1 ms in the wait test
 
-template <int KVT, int NT, class PP = AttnParams>
-__global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
+template <int KVT, int NT, class PP = AttnParams, bool kPair = false>
+__global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
+                                  AttnCfg<KVT, NT, kPair>::kMinBlocks)
     paged_attention_kernel(const __grid_constant__ CUtensorMap map, const PP p) {
-  using Cfg = AttnCfg<KVT, NT>;
+  using Cfg = AttnCfg<KVT, NT, kPair>;
   constexpr bool kPartial = IsPartial<PP>::value;
   constexpr bool kWaitTest = IsWaitTest<PP>::value;
   constexpr uint64_t kLimitNs = kWaitTest ? kTestWaitLimitNs : kWaitLimitNs;
@@ -382,6 +405,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
   volatile int* merge_flag = misc + 1;
   volatile int* has_frag = misc + 2;
   volatile int* frag_cnt = misc + 3;
+  volatile int* frag_first = misc + 4;    // first block of the fragment's segment (or -1)
   float* sWarp = reinterpret_cast<float*>(misc + 16);          // [W] per-warp scratch
   float* sMrow = sWarp + W;                                    // [RP]
   float* sLrow = sMrow + RP;                                   // [RP]
@@ -967,7 +991,11 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
           sML[(warp * 2 + 1) * RP + r] = l;
         }
       }
-    if (tid == 0) *frag_cnt = sp.count(f_seg, sf->a, sf->b);
+    if (tid == 0) {
+      int first;
+      *frag_cnt = sp.count_fast(f_seg, sf->a, sf->b, first);
+      *frag_first = first;
+    }
     __syncthreads();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -1087,6 +1115,8 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT>::kThreads, 1)
             for (int q = 0; q < sp.k; ++q)
               if ((int64_t)(q + 1) * np / sp.k > (int64_t)q * np / sp.k)
                 slots[nsl++] = f_seg * sp.k + q;
+          } else if (*frag_first >= 0) {
+            for (int q = 0; q < cnt; ++q) slots[nsl++] = f_seg + *frag_first + q;
           } else {
             for (int64_t x = sf->a; x < sf->b;) {
               const int cc = sp.cta_of(x);

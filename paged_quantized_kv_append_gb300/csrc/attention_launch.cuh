@@ -23,52 +23,56 @@ cudaError_t opt_in_smem(Kernel* kernel, int bytes, std::atomic<uint64_t>& done) 
   return e;
 }
 
-template <int KVT, int NT>
+template <int KVT, int NT, bool kPair = false>
 cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& map, int grid,
                                cudaStream_t stream) {
-  using Cfg = AttnCfg<KVT, NT>;
+  using Cfg = AttnCfg<KVT, NT, kPair>;
   static std::atomic<uint64_t> attr_done{0};
-  const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT>,
+  const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnParams, kPair>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done);
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<KVT, NT>
+  paged_attention_kernel<KVT, NT, AttnParams, kPair>
       <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
   return cudaGetLastError();
 }
 
-template <int KVT, int NT>
+template <int KVT, int NT, bool kPair = false>
 int blocks_per_sm_t(int num_seqs) {
-  using Cfg = AttnCfg<KVT, NT>;
+  using Cfg = AttnCfg<KVT, NT, kPair>;
   static std::atomic<uint64_t> attr_done{0};
-  if (opt_in_smem(paged_attention_kernel<KVT, NT>, Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done) !=
-      cudaSuccess)
+  if (opt_in_smem(paged_attention_kernel<KVT, NT, AttnParams, kPair>,
+                  Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<KVT, NT>,
-                                                    Cfg::kThreads,
-                                                    Cfg::smem_bytes(num_seqs)) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, paged_attention_kernel<KVT, NT, AttnParams, kPair>, Cfg::kThreads,
+          Cfg::smem_bytes(num_seqs)) != cudaSuccess)
     return 0;
   return n;
 }
 
-template <int KVT, int NT>
+template <int KVT, int NT, bool kPair = false>
 cudaError_t launch_attention_partial_t(const AttnPartialParams& p, const CUtensorMap& map,
                                        int grid, cudaStream_t stream) {
-  using Cfg = AttnCfg<KVT, NT>;
+  using Cfg = AttnCfg<KVT, NT, kPair>;
   static std::atomic<uint64_t> attr_done{0};
-  const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnPartialParams>,
+  const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnPartialParams, kPair>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done);
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<KVT, NT, AttnPartialParams>
+  paged_attention_kernel<KVT, NT, AttnPartialParams, kPair>
       <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
   return cudaGetLastError();
 }
 
+// pair: the 8-row decode as two 8-warp blocks per SM (8-bit formats only)
 template <int KVT>
 cudaError_t launch_attention_partial_dtype(const AttnPartialParams& p, const CUtensorMap& map,
-                                           int grid, int nt, cudaStream_t stream) {
+                                           int grid, int nt, bool pair, cudaStream_t stream) {
   switch (nt) {
-    case 1: return launch_attention_partial_t<KVT, 1>(p, map, grid, stream);
+    case 1:
+      if constexpr (KVT != PQKV_KV_FP16)
+        if (pair) return launch_attention_partial_t<KVT, 1, true>(p, map, grid, stream);
+      return launch_attention_partial_t<KVT, 1>(p, map, grid, stream);
     case 2: return launch_attention_partial_t<KVT, 2>(p, map, grid, stream);
     case 3: return launch_attention_partial_t<KVT, 3>(p, map, grid, stream);
     case 4: return launch_attention_partial_t<KVT, 4>(p, map, grid, stream);
@@ -78,9 +82,12 @@ cudaError_t launch_attention_partial_dtype(const AttnPartialParams& p, const CUt
 
 template <int KVT>
 cudaError_t launch_attention_dtype(const AttnParams& p, const CUtensorMap& map, int grid, int nt,
-                                   cudaStream_t stream) {
+                                   bool pair, cudaStream_t stream) {
   switch (nt) {
-    case 1: return launch_attention_t<KVT, 1>(p, map, grid, stream);
+    case 1:
+      if constexpr (KVT != PQKV_KV_FP16)
+        if (pair) return launch_attention_t<KVT, 1, true>(p, map, grid, stream);
+      return launch_attention_t<KVT, 1>(p, map, grid, stream);
     case 2: return launch_attention_t<KVT, 2>(p, map, grid, stream);
     case 3: return launch_attention_t<KVT, 3>(p, map, grid, stream);
     case 4: return launch_attention_t<KVT, 4>(p, map, grid, stream);
@@ -89,9 +96,12 @@ cudaError_t launch_attention_dtype(const AttnParams& p, const CUtensorMap& map, 
 }
 
 template <int KVT>
-int blocks_per_sm_dtype(int nt, int num_seqs) {
+int blocks_per_sm_dtype(int nt, bool pair, int num_seqs) {
   switch (nt) {
-    case 1: return blocks_per_sm_t<KVT, 1>(num_seqs);
+    case 1:
+      if constexpr (KVT != PQKV_KV_FP16)
+        if (pair) return blocks_per_sm_t<KVT, 1, true>(num_seqs);
+      return blocks_per_sm_t<KVT, 1>(num_seqs);
     case 2: return blocks_per_sm_t<KVT, 2>(num_seqs);
     case 3: return blocks_per_sm_t<KVT, 3>(num_seqs);
     case 4: return blocks_per_sm_t<KVT, 4>(num_seqs);

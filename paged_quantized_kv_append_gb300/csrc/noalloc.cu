@@ -82,6 +82,6 @@ extern "C" int pqkv_paged_attention_noalloc(const void* q, void* out, const void
     // start must be zero when the kernel begins.
     if (cudaMemsetAsync(scratch, 0, L.pl.counter_bytes, st) != cudaSuccess) return PQKV_ECUDA;
   }
-  return launch_attention(kv_dtype, p, map, L.grid, L.nt, st) == cudaSuccess ? PQKV_OK
+  return launch_attention(kv_dtype, p, map, L.grid, L.nt, L.pair, st) == cudaSuccess ? PQKV_OK
                                                                               : PQKV_ECUDA;
 }

@@ -77,28 +77,33 @@ struct AttnWaitTestParams : AttnParams {
 
 // Host launchers (one per KV format), defined in the attention translation units.
 cudaError_t launch_attention_fp16(const AttnParams& p, const CUtensorMap& map, int grid,
-                                  int nt, cudaStream_t stream);
+                                  int nt, bool pair, cudaStream_t stream);
 cudaError_t launch_attention_e4m3(const AttnParams& p, const CUtensorMap& map, int grid,
-                                  int nt, cudaStream_t stream);
+                                  int nt, bool pair, cudaStream_t stream);
 cudaError_t launch_attention_int8(const AttnParams& p, const CUtensorMap& map, int grid,
-                                  int nt, cudaStream_t stream);
+                                  int nt, bool pair, cudaStream_t stream);
 cudaError_t launch_attention_int8_row(const AttnParams& p, const CUtensorMap& map, int grid,
-                                      int nt, cudaStream_t stream);
+                                      int nt, bool pair, cudaStream_t stream);
 // Resident blocks per SM of the attention kernel for a KV format, n-tile
-// count and number of sequences (0 if the query fails).
-int attention_blocks_per_sm_fp16(int nt, int num_seqs);
-int attention_blocks_per_sm_e4m3(int nt, int num_seqs);
-int attention_blocks_per_sm_int8(int nt, int num_seqs);
-int attention_blocks_per_sm_int8_row(int nt, int num_seqs);
+// count, block shape (pair: the 8-row decode as two 8-warp blocks per SM)
+// and number of sequences (0 if the query fails).
+int attention_blocks_per_sm_fp16(int nt, bool pair, int num_seqs);
+int attention_blocks_per_sm_e4m3(int nt, bool pair, int num_seqs);
+int attention_blocks_per_sm_int8(int nt, bool pair, int num_seqs);
+int attention_blocks_per_sm_int8_row(int nt, bool pair, int num_seqs);
 
 cudaError_t launch_attention_partial_fp16(const AttnPartialParams& p, const CUtensorMap& map,
-                                          int grid, int nt, cudaStream_t stream);
+                                          int grid, int nt, bool pair,
+                                          cudaStream_t stream);
 cudaError_t launch_attention_partial_e4m3(const AttnPartialParams& p, const CUtensorMap& map,
-                                          int grid, int nt, cudaStream_t stream);
+                                          int grid, int nt, bool pair,
+                                          cudaStream_t stream);
 cudaError_t launch_attention_partial_int8(const AttnPartialParams& p, const CUtensorMap& map,
-                                          int grid, int nt, cudaStream_t stream);
+                                          int grid, int nt, bool pair,
+                                          cudaStream_t stream);
 cudaError_t launch_attention_partial_int8_row(const AttnPartialParams& p, const CUtensorMap& map,
-                                              int grid, int nt, cudaStream_t stream);
+                                              int grid, int nt, bool pair,
+                                          cudaStream_t stream);
 cudaError_t launch_attention_wait_test_e4m3(const AttnWaitTestParams& p, const CUtensorMap& map,
                                             int grid, int nt, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int num_parts,
@@ -132,9 +137,12 @@ struct AttnPlan {
   size_t counter_bytes = 0, o_bytes = 0, ml_bytes = 0, total = 0;
 };
 
-// Launch shape of one validated call: grid, row tiles and the workspace it needs.
+// Launch shape of one validated call: grid, row tiles, block shape (pair: the
+// 8-row decode of a short context as two 8-warp blocks per SM) and the
+// workspace it needs.
 struct AttnLaunch {
   int grid = 0, nt = 0, rows = 0;
+  bool pair = false;
   AttnPlan pl;
 };
 
@@ -148,7 +156,7 @@ int bind_attention(const AttnArgs& a, const AttnLaunch& L, void* workspace,
                    size_t workspace_bytes, int32_t* status, AttnParams* p, CUtensorMap* map);
 // Launch the attention kernel of the pool's format.
 cudaError_t launch_attention(int kv_dtype, const AttnParams& p, const CUtensorMap& map, int grid,
-                             int nt, cudaStream_t stream);
+                             int nt, bool pair, cudaStream_t stream);
 // PQKV_EINVAL (after the size checks) when num_seqs > 0 and an output
 // argument is missing or misaligned.
 int check_output_args(const AttnArgs& a, bool bad_outputs);
