@@ -256,13 +256,35 @@ def cpu_cores():
 
 
 def blas_threads():
-    """Threads of the BLAS / OpenMP pools numpy runs the oracle's products on
-    (the largest pool), or None when it cannot be queried."""
+    """Threads of the BLAS pool numpy runs the oracle's products on, or None
+    when it cannot be queried: threadpoolctl when installed, else the thread
+    count the loaded OpenBLAS library reports about itself."""
+    import ctypes
+    import numpy  # noqa: F401  (loads numpy's BLAS before it is inspected)
     try:
         from threadpoolctl import threadpool_info
-        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        pools = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if pools:
+            return max(pools)
     except Exception:
+        pass
+    try:
+        paths = {line.split()[-1] for line in open("/proc/self/maps")
+                 if "openblas" in line.lower() and ".so" in line}
+    except OSError:
         return None
+    for path in sorted(paths):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                    "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
 
 
 class OracleSample:
