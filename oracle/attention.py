@@ -127,12 +127,13 @@ def _scale_of(scale, h):
     return a[h] if a.size > 1 else a[0]
 
 
-def attention_partial(qrows, K, V, limits, j0, j1):
+def attention_partial(qrows, K, V, limits, j0, j1, lower=None):
     """Partial softmax state of query rows over keys [j0, j1).
 
     qrows: float64 [R, D]; K, V: float64 [L, D]; limits[r]: last key position
-    row r may see.  Returns (O [R, D], m [R], l [R]) with natural-log scores;
-    rows that see no key of the range get m = -inf, l = 0, O = 0.
+    row r may see; lower[r] (optional): first key position row r may see.
+    Returns (O [R, D], m [R], l [R]) with natural-log scores; rows that see no
+    key of the range get m = -inf, l = 0, O = 0.
     """
     D = qrows.shape[1]
     R = qrows.shape[0]
@@ -144,6 +145,8 @@ def attention_partial(qrows, K, V, limits, j0, j1):
     S = (qrows @ K[j0:j1].T) / np.sqrt(D)
     pos = np.arange(j0, j1)
     visible = pos[None, :] <= np.asarray(limits)[:, None]
+    if lower is not None:
+        visible &= pos[None, :] >= np.asarray(lower)[:, None]
     S = np.where(visible, S, -np.inf)
     for r in range(R):
         if not visible[r].any():
@@ -173,12 +176,15 @@ def _rows_of(q, s, h, q_len, G):
 
 
 def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v_scale,
-                    num_splits=1, seqs=None, heads=None):
+                    num_splits=1, seqs=None, heads=None, window=0):
     """float64 attention output [B * q_len, Hq, D] (rows of sequences / heads
     not selected by ``seqs`` / ``heads`` are left NaN).
 
     ``num_splits`` > 1 cuts every sequence's key range into that many
-    near-equal partitions and merges them by log-sum-exp.
+    near-equal partitions and merges them by log-sum-exp.  ``window`` > 0
+    limits query position p to the ``window`` most recent keys, itself
+    included: keys p - window + 1 .. p (ReVolta README, "DFlash2 speculative
+    decoding": sliding-window layers with a 2048-token window).
     """
     q = np.asarray(q)
     BQ, Hq, D = q.shape
@@ -189,6 +195,7 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
     for s in (range(B) if seqs is None else seqs):
         L = int(seq_lens[s])
         limits = np.repeat(L - q_len + np.arange(q_len), G)
+        lower = limits - window + 1 if window > 0 else None
         for h in (range(H) if heads is None else heads):
             if kv_dtype == INT8_TOKEN:
                 K, V = gather_kv(pages, block_table[s], L, h, kv_dtype, k_scale, v_scale)
@@ -197,7 +204,7 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
                                  _scale_of(k_scale, h), _scale_of(v_scale, h))
             rows = _rows_of(q, s, h, q_len, G)
             bounds = [(L * p) // num_splits for p in range(num_splits + 1)]
-            parts = [attention_partial(rows, K, V, limits, bounds[p], bounds[p + 1])
+            parts = [attention_partial(rows, K, V, limits, bounds[p], bounds[p + 1], lower)
                      for p in range(num_splits)]
             o = lse_merge(parts).reshape(q_len, G, D)
             out[s * q_len:(s + 1) * q_len, h * G:(h + 1) * G] = o
