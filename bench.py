@@ -442,19 +442,37 @@ def _rate(nbytes, us, peak):
     return {"us_per_step": us, "gbs": gbs, "frac_of_hbm": gbs / peak}
 
 
-def config_entry(pq, W, ctx, peak, flush=None, headline=None):
+def window_bytes(w, window):
+    """Algorithmic bytes of a sliding-window attention launch: K and V codes of
+    the keys some query's window holds (keys L - q_len - window + 1 .. L - 1
+    of each sequence), q, out, the block-table entries of the pages read, and
+    seq_lens."""
+    kv = toks = pages = 0
+    for L in w.seq_lens:
+        lo = max(0, L - w.q_len - window + 1)
+        toks += L - lo
+        pages += w.pages_of(L) - lo // w.page_size
+    kv = toks * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
+    q_bytes = w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * 2
+    return kv + 2 * q_bytes + pages * 4 + w.num_seqs * 4
+
+
+def config_entry(pq, W, ctx, peak, flush=None, headline=None, window=0):
     """One workload's figures: the step (append if the workload appends every
     step, then attention) and the attention alone, each a CUDA graph of
     back-to-back launches replayed for at least CONFIG_MIN_S; with `flush`,
-    also the same launches after an L2 flush (flush + launch minus flush)."""
+    also the same launches after an L2 flush (flush + launch minus flush).
+    `window` > 0 times the sliding-window attention instead (no append)."""
     w = ctx["w"]
     attn_bytes, app_bytes = algorithmic_bytes(ctx)
-    step_appends = bool(w.append_per_step) or bool(w.append_tokens)
+    step_appends = (bool(w.append_per_step) or bool(w.append_tokens)) and not window
+    if window:
+        attn_bytes = window_bytes(w, window)
 
     def attention():
         pq.paged_attention(ctx["q"], ctx["pages"], ctx["bt"], ctx["seq_lens"], w.q_len,
                            w.kv_dtype, ctx["ks"], ctx["vs"], ctx["out"], workspace=ctx["ws"],
-                           max_seq_len=max(w.seq_lens))
+                           max_seq_len=max(w.seq_lens), window=window)
 
     def append():
         pq.kv_append_quant(ctx["ak"], ctx["av"], ctx["aslots"], w.kv_dtype, ctx["ks"], ctx["vs"],
@@ -470,7 +488,7 @@ def config_entry(pq, W, ctx, peak, flush=None, headline=None):
         windows.append(win)
     else:
         attn_us = step_us
-    e = {"workload": w.name,
+    e = {"workload": w.name + ("_window%d" % window if window else ""),
          "shape": "%s x %s tokens, %d/%d heads, q_len %d, %s" % (
              w.num_seqs, (w.seq_lens[0] if len(set(w.seq_lens)) == 1 else
                           "%d..%d" % (min(w.seq_lens), max(w.seq_lens))),
@@ -481,6 +499,8 @@ def config_entry(pq, W, ctx, peak, flush=None, headline=None):
          "attention_bytes": attn_bytes, "append_bytes": app_bytes if step_appends else 0,
          "l2": "warm: back-to-back launches on the same inputs" if flush else
                "inputs larger than L2 (%.2f GB of KV)" % (w.kv_bytes() / 1e9)}
+    if window:
+        e["window"] = window
     e.update(_rate(attn_bytes + (app_bytes if step_appends else 0), step_us, peak))
     e["attention_us"] = attn_us
     e["attention_frac_of_hbm"] = attn_bytes / (attn_us * 1e-6) / 1e9 / peak
@@ -556,6 +576,10 @@ def per_config(pq, W, device, peak, headline_ctx, headline_us):
         ctx = setup(name, device)
         small = ctx["w"].kv_bytes() < 2 * flush.l2
         out[name] = config_entry(pq, W, ctx, peak, flush=flush if small else None)
+        if name == "e4m3_verify_131k":
+            # the same verify restricted to a 2048-token sliding window
+            e = config_entry(pq, W, ctx, peak, flush=flush, window=2048)
+            out[e["workload"]] = e
         del ctx
         gc.collect()
         torch.cuda.empty_cache()

@@ -197,6 +197,29 @@ int pqkv_paged_attention(const void* q, void* out, const void* pages, int64_t nu
                          int32_t* status, void* stream);
 
 /*
+ * pqkv_paged_attention_window -- pqkv_paged_attention with a sliding window:
+ * query position p attends to the `window` most recent keys, itself included,
+ * i.e. keys j with p - window < j <= p.  (ReVolta README, "DFlash2
+ * speculative decoding": the drafter's sliding-window layers use a 2048-token
+ * window.)  Pages that lie wholly before every query's window are not read, so
+ * the cost follows the window, not the cache length.
+ *
+ * Same arguments as pqkv_paged_attention, plus:
+ *   window   >= 1: the window in tokens; 0: no window (exactly
+ *            pqkv_paged_attention); negative: PQKV_EINVAL.
+ * The workspace rules are those of pqkv_paged_attention (its size query
+ * covers this call).
+ */
+int pqkv_paged_attention_window(const void* q, void* out, const void* pages, int64_t num_pages,
+                                const int32_t* block_table, int32_t max_pages_per_seq,
+                                const int32_t* seq_lens, int32_t num_seqs, int32_t q_len,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t page_size, int32_t kv_dtype, const float* k_scale,
+                                const float* v_scale, int32_t scale_per_head, int32_t num_splits,
+                                int32_t max_seq_len, int32_t window, void* workspace,
+                                size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * pqkv_paged_attention_partial -- one rank's part of a decode context
  * parallel split (ReVolta README, "Hardware": TP4 + DCP2; "Quick start",
  * launch: --decode-context-parallel-size 2): each rank holds a contiguous,

@@ -68,6 +68,11 @@ def load_library(path: str | None = None):
         lib.pqkv_paged_attention.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_vp, c_i32,
                                              c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp,
                                              c_i32, c_i32, c_i32, c_vp, c_sz, c_vp, c_vp]
+        lib.pqkv_paged_attention_window.restype = ctypes.c_int
+        lib.pqkv_paged_attention_window.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_vp,
+                                                    c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                                    c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
+                                                    c_vp, c_sz, c_vp, c_vp]
         lib.pqkv_paged_attention_noalloc.restype = ctypes.c_int
         lib.pqkv_paged_attention_noalloc.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_i32, c_vp,
                                                      c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
@@ -252,13 +257,15 @@ def _default_workspace(device):
 
 
 def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v_scale, out,
-                    num_splits=0, max_seq_len=0, workspace=None, status=None, stream=None):
+                    num_splits=0, max_seq_len=0, workspace=None, status=None, stream=None,
+                    window=0):
     """Decode (q_len 1) or verify (q_len > 1) attention over the paged pool.
 
     q, out: fp16 [num_seqs * q_len, Hq, 128]; block_table: int32
     [num_seqs, max_pages_per_seq]; seq_lens: int32 [num_seqs] (cached tokens,
     the q_len new ones included).  num_splits 0 balances key pages over the
-    GPU; k >= 1 cuts each (sequence, kv-head) into k partitions.
+    GPU; k >= 1 cuts each (sequence, kv-head) into k partitions.  window > 0:
+    query position p sees only keys p - window + 1 .. p (sliding window).
     """
     kd = _dtype_id(kv_dtype)
     _check_pages(pages, kd)
@@ -293,12 +300,22 @@ def paged_attention(q, pages, block_table, seq_lens, q_len, kv_dtype, k_scale, v
     _on_device(dev, workspace=ws)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     lib = load_library()
+    if window < 0:
+        raise ValueError("window must be >= 0")
     with torch.cuda.device(dev):
-        rc = lib.pqkv_paged_attention(
-            _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table),
-            block_table.shape[1], _ptr(seq_lens), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
-            _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None),
-            sph, num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
+        if window > 0:
+            rc = lib.pqkv_paged_attention_window(
+                _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table),
+                block_table.shape[1], _ptr(seq_lens), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
+                _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None),
+                sph, num_splits, max_seq_len, window, _ptr(ws), ws_bytes, _ptr(status),
+                _stream(q, stream))
+        else:
+            rc = lib.pqkv_paged_attention(
+                _ptr(q), _ptr(out), _ptr(pages), pages.shape[0], _ptr(block_table),
+                block_table.shape[1], _ptr(seq_lens), B, q_len, Hq, H, HEAD_DIM, PAGE_SIZE, kd,
+                _ptr(k_scale if kd in _SCALED else None), _ptr(v_scale if kd in _SCALED else None),
+                sph, num_splits, max_seq_len, _ptr(ws), ws_bytes, _ptr(status), _stream(q, stream))
     _check(rc, "paged_attention")
     return out
 

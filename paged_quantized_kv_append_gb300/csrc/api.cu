@@ -218,10 +218,15 @@ int plan_attention_launch(const AttnArgs& a, AttnLaunch* L) {
   bool pair = false;
   if (a.num_splits == 0) {
     const int64_t cap_len = (int64_t)a.max_pages_per_seq * a.page_size;
-    const int64_t lmax = a.max_seq_len > 0 ? std::min<int64_t>(a.max_seq_len, cap_len) : cap_len;
+    int64_t lmax = a.max_seq_len > 0 ? std::min<int64_t>(a.max_seq_len, cap_len) : cap_len;
+    // a sliding window reads at most window + q_len - 1 keys per sequence,
+    // over one page more than they fill
+    if (a.window > 0)
+      lmax = std::min<int64_t>(lmax, (int64_t)a.window + a.q_len - 1 + a.page_size);
     const int64_t units =
         (int64_t)a.num_seqs * a.num_kv_heads * ((lmax + a.page_size - 1) / a.page_size);
-    pair = nt == 1 && a.kv_dtype != PQKV_KV_FP16 && units <= kPairMaxUnitsPerSm * sms;
+    pair = nt == 1 && a.kv_dtype != PQKV_KV_FP16 && a.window == 0 &&
+           units <= kPairMaxUnitsPerSm * sms;
     const int per_sm = blocks_per_sm(a.kv_dtype, nt, pair, a.num_seqs);
     if (per_sm <= 0) return PQKV_ECUDA;
     const int64_t want = (units + kMinPagesPerBlock - 1) / kMinPagesPerBlock;
@@ -344,6 +349,49 @@ extern "C" int pqkv_paged_attention(const void* q, void* out, const void* pages,
   p.out = static_cast<uint16_t*>(out);
   const cudaError_t e =
       launch_attention(kv_dtype, p, map, L.grid, L.nt, L.pair, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
+}
+
+extern "C" int pqkv_paged_attention_window(const void* q, void* out, const void* pages,
+                                           int64_t num_pages, const int32_t* block_table,
+                                           int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                           int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t page_size, int32_t kv_dtype,
+                                           const float* k_scale, const float* v_scale,
+                                           int32_t scale_per_head, int32_t num_splits,
+                                           int32_t max_seq_len, int32_t window, void* workspace,
+                                           size_t workspace_bytes, int32_t* status, void* stream) {
+  AttnArgs a{q, pages, num_pages, block_table, max_pages_per_seq, seq_lens, num_seqs, q_len,
+             num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype, k_scale, v_scale,
+             scale_per_head, num_splits, max_seq_len};
+  int rc = check_output_args(a, !out || !aligned(out, 16));
+  if (rc) return rc;
+  if (window < 0) return PQKV_EINVAL;
+  if (window == 0)      // no window: the plain kernel
+    return pqkv_paged_attention(q, out, pages, num_pages, block_table, max_pages_per_seq,
+                                seq_lens, num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
+                                page_size, kv_dtype, k_scale, v_scale, scale_per_head,
+                                num_splits, max_seq_len, workspace, workspace_bytes, status,
+                                stream);
+  a.window = window;
+  AttnLaunch L;
+  rc = plan_attention_launch(a, &L);
+  if (rc || num_seqs == 0) return rc;
+  AttnWindowParams p;
+  CUtensorMap map;
+  rc = bind_attention(a, L, workspace, workspace_bytes, status, &p, &map);
+  if (rc) return rc;
+  p.out = static_cast<uint16_t*>(out);
+  p.window = window;
+  cudaError_t e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (kv_dtype) {
+    case PQKV_KV_FP16: e = launch_attention_window_fp16(p, map, L.grid, L.nt, st); break;
+    case PQKV_KV_FP8_E4M3: e = launch_attention_window_e4m3(p, map, L.grid, L.nt, st); break;
+    case PQKV_KV_INT8_ROW: e = launch_attention_window_int8_row(p, map, L.grid, L.nt, st); break;
+    default: e = launch_attention_window_int8(p, map, L.grid, L.nt, st); break;
+  }
   return e == cudaSuccess ? PQKV_OK : PQKV_ECUDA;
 }
 

@@ -18,4 +18,9 @@ cudaError_t launch_attention_partial_e4m3(const AttnPartialParams& p, const CUte
   return launch_attention_partial_dtype<PQKV_KV_FP8_E4M3>(p, map, grid, nt, pair, stream);
 }
 
+cudaError_t launch_attention_window_e4m3(const AttnWindowParams& p, const CUtensorMap& map,
+                                         int grid, int nt, cudaStream_t stream) {
+  return launch_attention_window_dtype<PQKV_KV_FP8_E4M3>(p, map, grid, nt, stream);
+}
+
 }  // namespace pqkv

@@ -42,7 +42,7 @@
 
 namespace pqkv {
 
-template <int KVT, int NT, bool kPair = false>
+template <int KVT, int NT, bool kPair = false, bool kWideTree = false>
 struct AttnCfg {
   // One block per SM.  Every warp is a consumer and feeds its own slice of the
   // TMA ring: page i of the block goes to warp i % kW and stage i % kStages,
@@ -65,7 +65,9 @@ struct AttnCfg {
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
   static constexpr int kTileBytes = kLines * 128;
   static constexpr int kStagesPerWarp =
-      (KVT == PQKV_KV_FP16 || kPair) ? 2 : (kW <= 8 ? 4 : (kW == 12 ? 3 : 2));
+      (KVT == PQKV_KV_FP16 || kPair || (kWideTree && (NT == 2 || NT == 4)))
+          ? 2
+          : (kW <= 8 ? 4 : (kW == 12 ? 3 : 2));
   static constexpr int kStages = kW * kStagesPerWarp;
   static constexpr int kRP = 8 * NT;                               // padded query rows
   static constexpr int kQfBytes = 8 * NT * 32 * 8;
@@ -79,7 +81,10 @@ struct AttnCfg {
   // buffer (8 warps: one group), then the group buffers are added in fixed
   // order -- the 24-row page loop compiled slower with the tree epilogue,
   // and the 32-row kernel has no shared memory left for its buffers.
-  static constexpr bool kTree = NT <= 2;
+  // kWideTree: the sliding-window kernel, a separate instantiation: the tree
+  // for 24 and 32 rows too (8-bit formats), and two ring stages per warp for
+  // 16 and 32 rows so its buffers and per-sequence array fit
+  static constexpr bool kTree = NT <= 2 || (kWideTree && KVT != PQKV_KV_FP16);
   static constexpr int kCombGroups = kW >= 12 ? kW / 4 : 1;
   static constexpr int kCombSize = kW / kCombGroups;
   static constexpr int kOBytes = kRP * kHeadDim * 4;     // one buffer
@@ -104,6 +109,10 @@ struct AttnCfg {
     return kPreOff + (2 * num_seqs + 1) * 4 + 1024;
   }
   static_assert(kStages % kW == 0, "each ring stage must belong to one warp");
+  // the largest launch (PQKV_MAX_SEQS sequences; the sliding-window kernel
+  // also keeps one int per sequence) fits the 227 KB a block may opt into
+  static_assert(smem_bytes(PQKV_MAX_SEQS) + (kWideTree ? 4 * PQKV_MAX_SEQS : 0) <= 232448,
+                "shared memory of the largest launch");
   static_assert(kW % kCombGroups == 0, "whole combine groups");
   static_assert(kOBytes / 4 >= 1024, "the merge's slot list (<= 1024 blocks) must fit the O buffer");
 };
@@ -379,15 +388,18 @@ template <class PP> struct IsPartial { static constexpr bool value = false; };
 template <> struct IsPartial<AttnPartialParams> { static constexpr bool value = true; };
 template <class PP> struct IsWaitTest { static constexpr bool value = false; };
 template <> struct IsWaitTest<AttnWaitTestParams> { static constexpr bool value = true; };
+template <class PP> struct IsWindow { static constexpr bool value = false; };
+template <> struct IsWindow<AttnWindowParams> { static constexpr bool value = true; };
 constexpr uint64_t kTestWaitLimitNs = 1000000ull;   // 1 ms in the wait test
 
 template <int KVT, int NT, class PP = AttnParams, bool kPair = false>
 __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
                                   AttnCfg<KVT, NT, kPair>::kMinBlocks)
     paged_attention_kernel(const __grid_constant__ CUtensorMap map, const PP p) {
-  using Cfg = AttnCfg<KVT, NT, kPair>;
+  using Cfg = AttnCfg<KVT, NT, kPair, IsWindow<PP>::value>;
   constexpr bool kPartial = IsPartial<PP>::value;
   constexpr bool kWaitTest = IsWaitTest<PP>::value;
+  constexpr bool kWin = IsWindow<PP>::value;
   constexpr uint64_t kLimitNs = kWaitTest ? kTestWaitLimitNs : kWaitLimitNs;
   constexpr int W = Cfg::kW, S = Cfg::kStages, SPW = Cfg::kStagesPerWarp, RP = Cfg::kRP;
   constexpr int nthr = W * 32;
@@ -414,6 +426,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   int* pre = reinterpret_cast<int*>(smem + Cfg::kPreOff);
   int* sLim = reinterpret_cast<int*>(smem + Cfg::kPreOff - RP * 4);   // [RP] if kRowsInSmem
   int* slen = pre + p.num_seqs + 1;
+  int* sfp = slen + p.num_seqs;     // sliding window: each sequence's first page read
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -430,6 +443,12 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     }
     slen[s] = L;
     pre[s + 1] = (L + kPageSize - 1) / kPageSize;
+    if constexpr (kWin) {
+      // the first key any query of the sequence sees, and its page
+      const int fp = max(0, L - p.q_len - p.window + 1) / kPageSize;
+      sfp[s] = fp;
+      pre[s + 1] -= fp;
+    }
   }
   if (tid == 0) {
     pre[0] = 0;
@@ -509,7 +528,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     const int64_t off = x - (int64_t)pre[lo] * H;
     h = (int)(off / np);
     const int pg = (int)(off % np);
-    id = __ldg(p.block_table + (int64_t)lo * p.bt_stride + pg);
+    if constexpr (kWin)
+      id = __ldg(p.block_table + (int64_t)lo * p.bt_stride + sfp[lo] + pg);
+    else
+      id = __ldg(p.block_table + (int64_t)lo * p.bt_stride + pg);
     if (id < 0 || (int64_t)id >= p.num_pages) report(p.status, PQKV_DEV_PAGE_RANGE);
   };
   int cur_id, cur_h, nxt_id, nxt_h, ubase = 0;
@@ -674,7 +696,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
       }
       if (dead) continue;
       const uint8_t* T = ring + stage * Cfg::kTileBytes;
-      const int pos0 = (f_pg0 + j) * kPageSize;
+      const int pos0 = (kWin ? sfp[f_s] + f_pg0 + j : f_pg0 + j) * kPageSize;
 
       // S^T = K Q^T
       float sc[NT][4];
@@ -706,6 +728,19 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
             const int lm = Cfg::kRowsInSmem ? sLim[8 * nt + 2 * t + (e & 1)] : lim[nt][e & 1];
             if (tok > lm) sc[nt][e] = -INFINITY;
           }
+      }
+      if constexpr (kWin) {
+        // keys before a row's window: row r (limit lm) sees keys > lm - window
+        if (pos0 <= lim_min + p.q_len - 1 - p.window) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = pos0 + g + ((e & 2) ? 8 : 0);
+              const int lm = Cfg::kRowsInSmem ? sLim[8 * nt + 2 * t + (e & 1)] : lim[nt][e & 1];
+              if (tok <= lm - p.window) sc[nt][e] = -INFINITY;
+            }
+        }
       }
       // The reference maximum of a row only moves when one of its scores
       // exceeds it by more than 8 (probabilities then stay <= 2^8).  Each lane

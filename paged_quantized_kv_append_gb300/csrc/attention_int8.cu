@@ -18,4 +18,9 @@ cudaError_t launch_attention_partial_int8(const AttnPartialParams& p, const CUte
   return launch_attention_partial_dtype<PQKV_KV_INT8>(p, map, grid, nt, pair, stream);
 }
 
+cudaError_t launch_attention_window_int8(const AttnWindowParams& p, const CUtensorMap& map,
+                                         int grid, int nt, cudaStream_t stream) {
+  return launch_attention_window_dtype<PQKV_KV_INT8>(p, map, grid, nt, stream);
+}
+
 }  // namespace pqkv

@@ -64,6 +64,33 @@ cudaError_t launch_attention_partial_t(const AttnPartialParams& p, const CUtenso
   return cudaGetLastError();
 }
 
+// Sliding-window mode: the kernel also keeps each sequence's first page read
+// (num_seqs ints after the sequence lengths).
+template <int KVT, int NT>
+cudaError_t launch_attention_window_t(const AttnWindowParams& p, const CUtensorMap& map, int grid,
+                                      cudaStream_t stream) {
+  using Cfg = AttnCfg<KVT, NT, false, true>;
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnWindowParams>,
+                                    Cfg::smem_bytes(PQKV_MAX_SEQS) + 4 * PQKV_MAX_SEQS, attr_done);
+  if (e != cudaSuccess) return e;
+  paged_attention_kernel<KVT, NT, AttnWindowParams>
+      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs) + 4 * p.num_seqs, stream>>>(map, p);
+  return cudaGetLastError();
+}
+
+template <int KVT>
+cudaError_t launch_attention_window_dtype(const AttnWindowParams& p, const CUtensorMap& map,
+                                          int grid, int nt, cudaStream_t stream) {
+  switch (nt) {
+    case 1: return launch_attention_window_t<KVT, 1>(p, map, grid, stream);
+    case 2: return launch_attention_window_t<KVT, 2>(p, map, grid, stream);
+    case 3: return launch_attention_window_t<KVT, 3>(p, map, grid, stream);
+    case 4: return launch_attention_window_t<KVT, 4>(p, map, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 // pair: the 8-row decode as two 8-warp blocks per SM (8-bit formats only)
 template <int KVT>
 cudaError_t launch_attention_partial_dtype(const AttnPartialParams& p, const CUtensorMap& map,

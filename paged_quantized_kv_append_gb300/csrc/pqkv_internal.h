@@ -65,6 +65,12 @@ struct AttnPartialParams : AttnParams {
   float* out_lse;           // [B*q_len][Hq]
 };
 
+// Sliding-window attention: query position p sees keys p - window + 1 .. p
+// (window >= 1); the pages wholly before every query's window are never read.
+struct AttnWindowParams : AttnParams {
+  int32_t window;
+};
+
 // Test mode of the bounded waits: the feed of block `skip_block` does not
 // issue the copy of that block's page `skip_page` (its position in the
 // block's share), so the warp that owns the page waits for a tile that never
@@ -104,6 +110,14 @@ cudaError_t launch_attention_partial_int8(const AttnPartialParams& p, const CUte
 cudaError_t launch_attention_partial_int8_row(const AttnPartialParams& p, const CUtensorMap& map,
                                               int grid, int nt, bool pair,
                                           cudaStream_t stream);
+cudaError_t launch_attention_window_fp16(const AttnWindowParams& p, const CUtensorMap& map,
+                                         int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_window_e4m3(const AttnWindowParams& p, const CUtensorMap& map,
+                                         int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_window_int8(const AttnWindowParams& p, const CUtensorMap& map,
+                                         int grid, int nt, cudaStream_t stream);
+cudaError_t launch_attention_window_int8_row(const AttnWindowParams& p, const CUtensorMap& map,
+                                             int grid, int nt, cudaStream_t stream);
 cudaError_t launch_attention_wait_test_e4m3(const AttnWaitTestParams& p, const CUtensorMap& map,
                                             int grid, int nt, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int num_parts,
@@ -128,6 +142,7 @@ struct AttnArgs {
   const float* k_scale;
   const float* v_scale;
   int32_t scale_per_head, num_splits, max_seq_len;
+  int32_t window = 0;       // sliding window (0: none); only sizes the grid here
 };
 
 // Workspace carve-up of one call: merge counters, partial O, partial (m, l).

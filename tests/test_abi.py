@@ -104,6 +104,28 @@ def _attn(lib, **kw):
                                     a["ws"], a["wsb"], None, None)
 
 
+def _attn_window(lib, window, **kw):
+    a = dict(q=1 << 12, out=1 << 12, pages=1 << 12, npages=100, bt=1 << 12, mpps=8,
+             sl=1 << 12, B=2, qlen=5, hq=32, hkv=8, D=128, P=16, dt=1, kscale=1 << 12,
+             vscale=1 << 12, sph=0, ns=1, msl=0, ws=None, wsb=0)
+    a.update(kw)
+    return lib.pqkv_paged_attention_window(a["q"], a["out"], a["pages"], a["npages"], a["bt"],
+                                           a["mpps"], a["sl"], a["B"], a["qlen"], a["hq"],
+                                           a["hkv"], a["D"], a["P"], a["dt"], a["kscale"],
+                                           a["vscale"], a["sph"], a["ns"], a["msl"], window,
+                                           a["ws"], a["wsb"], None, None)
+
+
+def test_window_entry_point_validation(lib):
+    assert _attn_window(lib, -1) == EINVAL
+    assert _attn_window(lib, 16, D=256) == EUNSUPPORTED
+    assert _attn_window(lib, 16, qlen=9) == ERANGE
+    assert _attn_window(lib, 16, out=None) == EINVAL
+    assert _attn_window(lib, 16, B=0) == OK               # nothing to do, no CUDA call
+    assert _attn_window(lib, 0) == ECUDA                  # no window: the plain call (no GPU)
+    assert _attn_window(lib, 2048) == ECUDA               # valid, but no GPU here
+
+
 def test_attention_validation(lib):
     assert _attn(lib, D=256) == EUNSUPPORTED
     assert _attn(lib, hq=30) == EINVAL                    # Hq % Hkv != 0

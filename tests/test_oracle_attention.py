@@ -261,15 +261,16 @@ def test_planted_mistakes_are_caught(monkeypatch):
     # 1. softmax scale 1/D instead of 1/sqrt(D)
     orig_partial = oatt.attention_partial
 
-    def bad_scale(qrows, K, V, limits, j0, j1):
-        return orig_partial(qrows / np.sqrt(qrows.shape[1]), K, V, limits, j0, j1)
+    def bad_scale(qrows, K, V, limits, j0, j1, lower=None):
+        return orig_partial(qrows / np.sqrt(qrows.shape[1]), K, V, limits, j0, j1, lower)
     monkeypatch.setattr(oatt, "attention_partial", bad_scale)
     assert not _pins_pass(pins)
     monkeypatch.setattr(oatt, "attention_partial", orig_partial)
 
     # 2. causal limit off by one
-    def bad_causal(qrows, K, V, limits, j0, j1):
-        return orig_partial(qrows, K, V, np.asarray(limits) + 1, j0, min(j1 + 1, K.shape[0]))
+    def bad_causal(qrows, K, V, limits, j0, j1, lower=None):
+        return orig_partial(qrows, K, V, np.asarray(limits) + 1, j0, min(j1 + 1, K.shape[0]),
+                            lower)
     monkeypatch.setattr(oatt, "attention_partial", bad_causal)
     assert not _pins_pass(pins)
     monkeypatch.setattr(oatt, "attention_partial", orig_partial)
