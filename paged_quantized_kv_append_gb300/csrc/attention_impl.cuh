@@ -60,6 +60,10 @@ struct AttnCfg {
   // block; the two blocks' start-up and fragment ends do not wait on each
   // other.
   static constexpr int kMinBlocks = kPair ? 2 : 1;
+  // paired short decodes balance cost, charging each segment boundary this
+  // many units: a fragment end, a query reload and, usually, the segment's
+  // merge (measured best among 1..220 on the 8-sequence E4M3 decode)
+  static constexpr int kFragUnits = kPair ? 60 : 0;
   static_assert(!kPair || (NT == 1 && KVT != PQKV_KV_FP16), "paired blocks: 8-row 8-bit decode only");
   static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
@@ -135,16 +139,62 @@ struct Frag {
   int64_t a, b;         // the segment's span in the concatenated list
 };
 
-struct Split {
+// kCost: the balanced shares equalise cost rather than units, where every
+// segment after the first adds F units of cost at its start.  A block whose
+// share crosses into the next segment pays a fragment end and a query reload;
+// charging them keeps such blocks from finishing last.  Deterministic: the
+// shares depend only on the sequence lengths and the grid.
+template <bool kCost> struct SplitCost {};
+template <> struct SplitCost<true> {
+  int F;                // cost units charged per segment boundary
+  int64_t Ctot;         // P + F * (B * H - 1)
+};
+
+template <bool kCost>
+struct SplitT : SplitCost<kCost> {
   const int* pre;       // [B + 1] page prefix per sequence
   int B, H;
   int64_t P;            // total (page, kv-head) units
   int C;                // blocks
   int k;                // 0 = balanced
 
-  __device__ __forceinline__ int64_t start(int c) const { return (int64_t)c * P / C; }
+  // cost of unit x: x plus F for every segment starting at or before x but
+  // the first (segments are never empty here: every sequence holds a key)
+  __device__ int64_t cost(int64_t x) const {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)pre[mid] * H <= x) lo = mid; else hi = mid - 1;
+    }
+    const int64_t h = (x - (int64_t)pre[lo] * H) / pages(lo);
+    return x + (int64_t)this->F * ((int64_t)lo * H + h);
+  }
+  // first unit of block c's share
+  __device__ int64_t start(int c) const {
+    if constexpr (!kCost) {
+      return (int64_t)c * P / C;
+    } else {
+      const int F = this->F;
+      if (c <= 0) return 0;
+      if (c >= C) return P;
+      const int64_t T = ((int64_t)c * this->Ctot + C - 1) / C;   // smallest cost in the share
+      int lo = 0, hi = B - 1;                                  // sequence of cost T
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)pre[mid] * H + (int64_t)F * mid * H <= T) lo = mid; else hi = mid - 1;
+      }
+      const int64_t base = (int64_t)pre[lo] * H, np = pages(lo);
+      const int64_t rel = T - base - (int64_t)F * lo * H;
+      const int64_t h = rel / (np + F), off = rel - h * (np + F);
+      if (h >= H) return (int64_t)pre[lo + 1] * H;           // cost between sequences
+      return base + h * np + (off < np ? off : np);           // in a segment, or just after it
+    }
+  }
   // the block whose (non-empty) share holds unit x
-  __device__ __forceinline__ int cta_of(int64_t x) const { return (int)(((x + 1) * C - 1) / P); }
+  __device__ __forceinline__ int cta_of(int64_t x) const {
+    if constexpr (!kCost) return (int)(((x + 1) * C - 1) / P);
+    else return (int)(cost(x) * C / this->Ctot);
+  }
   __device__ __forceinline__ int pages(int s) const { return pre[s + 1] - pre[s]; }
 
   // number of partial results of segment seg
@@ -162,7 +212,14 @@ struct Split {
       first = 0;
       return min(k, pages(seg / H));
     }
-    if (P < C) {
+    // with equal shares every share is non-empty when P >= C; with cost
+    // shares when every share spans at least F + 1 cost values (a share can
+    // then not fall inside the F-value gap a segment boundary adds);
+    // otherwise walk the blocks
+    bool walk;
+    if constexpr (kCost) walk = this->Ctot < (int64_t)(this->F + 1) * C;
+    else walk = P < C;
+    if (walk) {
       first = -1;
       return count(seg, a, b);
     }
@@ -171,14 +228,15 @@ struct Split {
   }
 };
 
-struct FragIter {
-  Split sp;
+template <bool kCost>
+struct FragIterT {
+  SplitT<kCost> sp;
   int c;
   int64_t x, e;
   int s;
   bool fixed_done;
 
-  __device__ void init(const Split& split, int cta) {
+  __device__ void init(const SplitT<kCost>& split, int cta) {
     sp = split;
     c = cta;
     s = 0;
@@ -223,7 +281,10 @@ struct FragIter {
   }
 };
 
-static_assert(sizeof(FragIter) + sizeof(Frag) <= 128, "iterator state must fit its smem slot");
+using Split = SplitT<false>;
+using FragIter = FragIterT<false>;
+
+static_assert(sizeof(FragIterT<true>) + sizeof(Frag) <= 128, "iterator state must fit its smem slot");
 
 // ---------------------------------------------------------------------------
 // Per-page work of one consumer warp
@@ -421,7 +482,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   float* sWarp = reinterpret_cast<float*>(misc + 16);          // [W] per-warp scratch
   float* sMrow = sWarp + W;                                    // [RP]
   float* sLrow = sMrow + RP;                                   // [RP]
-  FragIter* sit = reinterpret_cast<FragIter*>(sLrow + RP);
+  // paired short decodes (not the partial mode, where a sequence may hold no
+  // key) balance cost instead of units
+  constexpr bool kCostSplit = Cfg::kFragUnits > 0 && !kPartial && !kWin;
+  FragIterT<kCostSplit>* sit = reinterpret_cast<FragIterT<kCostSplit>*>(sLrow + RP);
   Frag* sf = reinterpret_cast<Frag*>(sit + 1);
   int* pre = reinterpret_cast<int*>(smem + Cfg::kPreOff);
   int* sLim = reinterpret_cast<int*>(smem + Cfg::kPreOff - RP * 4);   // [RP] if kRowsInSmem
@@ -483,13 +547,17 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     }
   }
 
-  Split sp;
+  SplitT<kCostSplit> sp;
   sp.pre = pre;
   sp.B = B;
   sp.H = H;
   sp.P = (int64_t)pre[B] * H;
   sp.C = gridDim.x;
   sp.k = p.num_splits;
+  if constexpr (kCostSplit) {
+    sp.F = Cfg::kFragUnits;
+    sp.Ctot = sp.P + (int64_t)sp.F * ((int64_t)B * H - 1);
+  }
 
   // -- this block's contiguous range [x0, x1) of the (page, kv-head) unit list
   int64_t x0 = 0, x1 = 0;
