@@ -46,6 +46,10 @@ def parse_args():
     ap.add_argument("--scale", type=float, default=1.0,
                     help="context-length scale of the workload (1.0 = the full workload; "
                          "smaller values are for profiling captures)")
+    ap.add_argument("--append-tokens", type=int, default=0,
+                    help="size of the step's append chunk for workloads that have one "
+                         "(default: the workload's own; e.g. 8192 with --scale 0.25 profiles "
+                         "the full-size append on a smaller pool)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
@@ -168,13 +172,15 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload set-up (seeded synthetic inputs, resident in HBM)
 # ---------------------------------------------------------------------------
-def setup(wname: str, device: str, scale: float = 1.0):
+def setup(wname: str, device: str, scale: float = 1.0, append_tokens: int = 0):
     import numpy as np
     import torch
     import paged_quantized_kv_append_gb300 as pq
     import workloads as W
 
     w = W.workload(wname, scale)
+    if append_tokens and w.append_tokens:
+        w.append_tokens = append_tokens      # a smaller pool with the full-size chunk
     plan = W.plan_pool(w)
     ks, vs = W.calibrated_scales(w, device)
     pages = pq.new_pages(plan.num_pages, w.num_kv_heads, w.kv_dtype, device, fill=0)
@@ -636,7 +642,7 @@ def run_pqkv(args, rank, local, world):
     pq.load_library()
     torch.cuda.set_device(local)
     dev = "cuda:%d" % local
-    ctx = setup(args.workload, dev, args.scale)
+    ctx = setup(args.workload, dev, args.scale, args.append_tokens)
     w = ctx["w"]
     stream = torch.cuda.current_stream()
     attn_bytes, app_bytes = algorithmic_bytes(ctx)

@@ -167,12 +167,14 @@ extern "C" int pqkv_kv_append_quant(const void* k, int64_t k_token_stride, const
   p.row_scales = kv_dtype == PQKV_KV_INT8_ROW ? row_scale_area(pages, num_pages, num_kv_heads)
                                               : nullptr;
   p.status = status;
-  // one pass when the chunk fits the resident threads (8 blocks of 256 per
-  // SM, two vectors per thread), grid-stride beyond that
+  // one pass when the chunk fits the resident blocks, grid-stride beyond
+  // that: at most one wave of the blocks that fit on every SM at once
+  const int per_sm = append_blocks_per_sm(kv_dtype);
+  if (per_sm < 1) return PQKV_ECUDA;
   const int64_t work = (int64_t)num_tokens * num_kv_heads * (kHeadDim / 16);
   const int64_t per_block = (int64_t)kAppendThreads * kAppendUnroll;
   const int64_t blocks = (work + per_block - 1) / per_block;
-  const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * 8);
+  const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * per_sm);
   if (launch_append(p, kv_dtype, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PQKV_ECUDA;
   return PQKV_OK;

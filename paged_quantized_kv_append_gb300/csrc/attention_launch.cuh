@@ -31,9 +31,14 @@ cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& map, int 
   const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnParams, kPair>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done);
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<KVT, NT, AttnParams, kPair>
-      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
-  return cudaGetLastError();
+  if constexpr (attention_uses_pdl<KVT, NT, AttnParams, kPair>()) {
+    return launch_pdl(paged_attention_kernel<KVT, NT, AttnParams, kPair>, grid, Cfg::kThreads,
+                      Cfg::smem_bytes(p.num_seqs), stream, map, p);
+  } else {
+    paged_attention_kernel<KVT, NT, AttnParams, kPair>
+        <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
+    return cudaGetLastError();
+  }
 }
 
 template <int KVT, int NT, bool kPair = false>
@@ -59,9 +64,8 @@ cudaError_t launch_attention_partial_t(const AttnPartialParams& p, const CUtenso
   const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnPartialParams, kPair>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done);
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<KVT, NT, AttnPartialParams, kPair>
-      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(paged_attention_kernel<KVT, NT, AttnPartialParams, kPair>, grid,
+                    Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream, map, p);
 }
 
 // Sliding-window mode: the kernel also keeps each sequence's first page read
@@ -74,9 +78,8 @@ cudaError_t launch_attention_window_t(const AttnWindowParams& p, const CUtensorM
   const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnWindowParams>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS) + 4 * PQKV_MAX_SEQS, attr_done);
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<KVT, NT, AttnWindowParams>
-      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs) + 4 * p.num_seqs, stream>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(paged_attention_kernel<KVT, NT, AttnWindowParams>, grid, Cfg::kThreads,
+                    Cfg::smem_bytes(p.num_seqs) + 4 * p.num_seqs, stream, map, p);
 }
 
 template <int KVT>

@@ -16,9 +16,8 @@ cudaError_t launch_attention_wait_test_e4m3(const AttnWaitTestParams& p, const C
   const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnWaitTestParams>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done);
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<KVT, NT, AttnWaitTestParams>
-      <<<grid, Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(paged_attention_kernel<KVT, NT, AttnWaitTestParams>, grid, Cfg::kThreads,
+                    Cfg::smem_bytes(p.num_seqs), stream, map, p);
 }
 
 }  // namespace pqkv

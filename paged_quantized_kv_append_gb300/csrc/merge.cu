@@ -12,6 +12,8 @@ namespace pqkv {
 __global__ void __launch_bounds__(256) lse_merge_kernel(const float* part_o, const float* part_lse,
                                                         int num_parts, int64_t rows,
                                                         uint16_t* out, float* out_lse) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -46,9 +48,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* part_o, con
 cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int num_parts,
                              int64_t rows, uint16_t* out, float* out_lse, cudaStream_t stream) {
   const int64_t blocks = (rows + 7) / 8;
-  lse_merge_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part_o, part_lse, num_parts, rows, out,
-                                                         out_lse);
-  return cudaGetLastError();
+  return launch_pdl(lse_merge_kernel, (unsigned)blocks, 256, 0, stream, part_o, part_lse,
+                    num_parts, rows, out, out_lse);
 }
 
 }  // namespace pqkv

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pqkv_internal.h"
 
 namespace pqkv {
@@ -17,6 +19,42 @@ namespace pqkv {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void report(int32_t* status, int bit) {
   if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// The kernels of this library (all but one attention instantiation, see
+// attention_impl.cuh) are launched with programmatic stream serialization
+// allowed, so their blocks may become resident while the kernel before them
+// in the stream is still running.  Such a kernel waits, before its first
+// global-memory access, until that kernel has completed and its writes are
+// visible (at once when there is none), and then lets the next kernel's
+// blocks be scheduled: what is saved is the launch latency between kernels,
+// not any ordering.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host side: launch `kernel` with programmatic stream serialization allowed.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

@@ -125,10 +125,11 @@ cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int num
 
 // Append launch shape: blocks of kAppendThreads threads, each thread takes
 // kAppendUnroll 16-element vectors per pass with every load of the pass
-// issued before the first division (kAppendUnroll * 64 bytes in flight).
+// issued before the first encode (kAppendUnroll * 64 bytes in flight).
 constexpr int kAppendThreads = 256;
 constexpr int kAppendUnroll = 1;
 cudaError_t launch_append(const AppendParams& p, int kv_dtype, int grid, cudaStream_t stream);
+int append_blocks_per_sm(int kv_dtype);
 
 // The arguments of one attention call (the shared part of the entry points).
 struct AttnArgs {

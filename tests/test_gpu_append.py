@@ -45,8 +45,17 @@ def _run(kv_dtype, kvals, vvals, H, ks, vs, slots, num_pages, fill=0x5A, k_strid
     return got, ref, int(status.item())
 
 
+# Scales: powers of two (every quotient exact, so E4M3 midpoints and INT8
+# half-integers are hit exactly), calibrated amax / 448 and amax / 127 scales
+# (quotients that fall within an ulp of those boundaries), plain values, and
+# scales outside [2^-125, 2^125] where the encode takes the division.
+SCALES = [1.0, 86.625 / 448.0, 2.0 ** -7, 3.0, 1000.0, 0.3,
+          W.scale_from_amax(86.5, 448.0), W.scale_from_amax(86.5, 127.0),
+          W.scale_from_amax(7.0, 448.0), 2.0 ** -126, 2.0 ** 126, 1.5e-38]
+
+
 @pytest.mark.parametrize("kv_dtype", [W.FP8_E4M3, W.INT8])
-@pytest.mark.parametrize("scale", [1.0, 86.625 / 448.0, 2.0 ** -7, 3.0, 1000.0, 0.3])
+@pytest.mark.parametrize("scale", SCALES)
 def test_every_fp16_value_bit_exact(kv_dtype, scale):
     x = _all_fp16()
     T = len(x) // 128
