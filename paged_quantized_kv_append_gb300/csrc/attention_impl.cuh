@@ -62,10 +62,15 @@ struct AttnCfg {
   // block; the two blocks' start-up and fragment ends do not wait on each
   // other.
   static constexpr int kMinBlocks = kPair ? 2 : 1;
-  // paired short decodes balance cost, charging each segment boundary this
-  // many units: a fragment end, a query reload and, usually, the segment's
-  // merge (measured best among 1..220 on the 8-sequence E4M3 decode)
-  static constexpr int kFragUnits = kPair ? 60 : 0;
+  // Balanced shares that charge each segment boundary this many units (a
+  // fragment end, a query reload and, usually, the segment's merge): the
+  // paired short decodes (60, measured best among 1..220 on the 8-sequence
+  // E4M3 decode) and the 24-row INT8_ROW verify (120: 567 -> 556 us on the
+  // 131K verify).  The other kernels balance units: the same charge made the
+  // 24-row E4M3 verify's page loop compile 8 % slower, and the 32-row one
+  // gained nothing.
+  static constexpr int kFragUnits =
+      kPair ? 60 : ((KVT == PQKV_KV_INT8_ROW && NT == 3) ? 120 : 0);
   static_assert(!kPair || (NT == 1 && KVT != PQKV_KV_FP16), "paired blocks: 8-row 8-bit decode only");
   static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
