@@ -212,6 +212,29 @@ struct SplitT : SplitCost<kCost> {
     return n;
   }
 
+  // n / d for n >= 0, d > 0, in 32-bit arithmetic when both fit (a 64-bit
+  // division is a long dependent chain, and one thread computes these while
+  // the block waits at the fragment end)
+  static __device__ __forceinline__ int64_t udiv(int64_t n, int64_t d) {
+    if (((uint64_t)n | (uint64_t)d) <= 0xFFFFFFFFull) return (uint32_t)n / (uint32_t)d;
+    return n / d;
+  }
+  // cta_of with those divisions (the same values)
+  __device__ __forceinline__ int cta_of_q(int64_t x) const {
+    if constexpr (!kCost) {
+      return (int)udiv((x + 1) * C - 1, P);
+    } else {
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)pre[mid] * H <= x) lo = mid; else hi = mid - 1;
+      }
+      const int64_t h = udiv(x - (int64_t)pre[lo] * H, pages(lo));
+      const int64_t cx = x + (int64_t)this->F * ((int64_t)lo * H + h);
+      return (int)udiv(cx * C, this->Ctot);
+    }
+  }
+
   // The same in constant time when every block's share is non-empty (P >= C):
   // the blocks holding units of [a, b) are then exactly first .. first + n - 1.
   __device__ __forceinline__ int count_fast(int seg, int64_t a, int64_t b, int& first) const {
@@ -230,8 +253,8 @@ struct SplitT : SplitCost<kCost> {
       first = -1;
       return count(seg, a, b);
     }
-    first = cta_of(a);
-    return cta_of(b - 1) - first + 1;
+    first = cta_of_q(a);
+    return cta_of_q(b - 1) - first + 1;
   }
 };
 
@@ -453,12 +476,14 @@ __device__ __forceinline__ void page_pv(const uint8_t* T, int g, int t,
 // The kernel
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch (see pqkv_common.cuh) for every instantiation
-// but the plain 24-row E4M3 kernel, which is launched without it: with the
-// grid-dependency wait in it, its page loop compiled about 1 us (0.2 %)
-// slower, and its launches gained nothing from an early start.
+// but two, which are launched without it: the plain 24-row E4M3 kernel (with
+// the grid-dependency wait in it, its page loop compiled about 1 us slower,
+// and its launches gained nothing from an early start) and the paired
+// short-decode kernel (back-to-back decodes ran 0.3-0.5 us faster without).
 template <int KVT, int NT, class PP, bool kPair>
 constexpr bool attention_uses_pdl() {
-  return !(KVT == PQKV_KV_FP8_E4M3 && NT == 3 && !kPair && std::is_same<PP, AttnParams>::value);
+  constexpr bool kPlain = std::is_same<PP, AttnParams>::value;
+  return !(kPlain && ((KVT == PQKV_KV_FP8_E4M3 && NT == 3 && !kPair) || kPair));
 }
 
 template <class PP> struct IsPartial { static constexpr bool value = false; };
@@ -1220,15 +1245,20 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
         }
     }
         if (cnt > 1) {
-      __threadfence();
+      // warp 0's partial writes, ordered by the barrier before thread 0's
+      // release; the last block's acquire, then the barrier, orders its
+      // partial loads after every other block's release
       __syncthreads();
       if (tid == 0) {
-        const int ticket = atomicAdd(p.counters + f_seg, 1);
+        int ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(ticket)
+                     : "l"(p.counters + f_seg)
+                     : "memory");
         *merge_flag = (ticket == cnt - 1);
       }
       __syncthreads();
       if (*merge_flag) {
-        __threadfence();
         // gather the segment's partial slots (fixed order) into shared memory
         int* slots = reinterpret_cast<int*>(sO);
         if (tid == 0) {
