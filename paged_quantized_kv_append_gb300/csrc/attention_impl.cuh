@@ -65,12 +65,14 @@ struct AttnCfg {
   // Balanced shares that charge each segment boundary this many units (a
   // fragment end, a query reload and, usually, the segment's merge): the
   // paired short decodes (60, measured best among 1..220 on the 8-sequence
-  // E4M3 decode) and the 24-row INT8_ROW verify (120: 567 -> 556 us on the
-  // 131K verify).  The other kernels balance units: the same charge made the
-  // 24-row E4M3 verify's page loop compile 8 % slower, and the 32-row one
-  // gained nothing.
+  // E4M3 decode), the sliding-window kernels (60: the 131K verify with a
+  // 2048-token window 34.3 -> 30.9 us; from 130 on, the shares get too small
+  // for the constant-time partial count) and the 24-row INT8_ROW verify (120:
+  // 567 -> 556 us on the 131K verify).  The other kernels balance units: the
+  // same charge made the 24-row E4M3 verify's page loop compile 8 % slower,
+  // and the 32-row one gained nothing.
   static constexpr int kFragUnits =
-      kPair ? 60 : ((KVT == PQKV_KV_INT8_ROW && NT == 3) ? 120 : 0);
+      kPair ? 60 : ((KVT == PQKV_KV_INT8_ROW && NT == 3) ? 120 : (kWideTree ? 60 : 0));
   static_assert(!kPair || (NT == 1 && KVT != PQKV_KV_FP16), "paired blocks: 8-row 8-bit decode only");
   static constexpr int kThreads = kW * 32;
   static constexpr int kLines = (KVT == PQKV_KV_FP16) ? 64 : 32;   // 128-B lines per tile
@@ -523,9 +525,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   float* sWarp = reinterpret_cast<float*>(misc + 16);          // [W] per-warp scratch
   float* sMrow = sWarp + W;                                    // [RP]
   float* sLrow = sMrow + RP;                                   // [RP]
-  // paired short decodes (not the partial mode, where a sequence may hold no
-  // key) balance cost instead of units
-  constexpr bool kCostSplit = Cfg::kFragUnits > 0 && !kPartial && !kWin;
+  // cost shares (not in the partial mode, where a sequence may hold no key
+  // and a segment may be empty; in the sliding-window mode every sequence
+  // reads at least one page)
+  constexpr bool kCostSplit = Cfg::kFragUnits > 0 && !kPartial;
   FragIterT<kCostSplit>* sit = reinterpret_cast<FragIterT<kCostSplit>*>(sLrow + RP);
   Frag* sf = reinterpret_cast<Frag*>(sit + 1);
   int* pre = reinterpret_cast<int*>(smem + Cfg::kPreOff);
