@@ -1282,56 +1282,53 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
           }
         }
         __syncthreads();
-        // per-row maximum and normaliser: the (m, l) of eight partials are
-        // loaded at once and folded in with a running rescale
-        if (tid < p.rows) {
-          const int r = tid;
+        // One pass: thread (r, dq) loads the (m, l) and the float4 dq of row r
+        // of eight partials at once and folds them in with a running rescale
+        // (fixed order, so the result is deterministic).
+        for (int it = tid; it < p.rows * 32; it += nthr) {
+          const int r = it >> 5, dq = it & 31;
           float M = kNoScore, l = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
           for (int q0 = 0; q0 < cnt; q0 += 8) {
             float mq[8], lq[8];
+            float4 vq[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const bool in = q0 + k < cnt;
-              const float* ml = p.part_ml + (size_t)slots[in ? q0 + k : 0] * 2 * RP;
-              mq[k] = in ? __ldcg(ml + r) : kNoScore;
-              lq[k] = in ? __ldcg(ml + RP + r) : 0.f;
+              const size_t sl = slots[in ? q0 + k : 0];
+              mq[k] = in ? __ldcg(p.part_ml + sl * 2 * RP + r) : kNoScore;
+              lq[k] = in ? __ldcg(p.part_ml + sl * 2 * RP + RP + r) : 0.f;
+              vq[k] = in ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (sl * RP + r) *
+                                                                             kHeadDim) + dq)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             float Mn = M;
 #pragma unroll
             for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mq[k]);
-            l *= ex2(M - Mn);
+            const float f = ex2(M - Mn);
+            l *= f;
+            acc.x *= f;
+            acc.y *= f;
+            acc.z *= f;
+            acc.w *= f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) l += ex2(mq[k] - Mn) * lq[k];
+            for (int k = 0; k < 8; ++k) {
+              const float wq = ex2(mq[k] - Mn);
+              l += wq * lq[k];
+              acc.x += wq * vq[k].x;
+              acc.y += wq * vq[k].y;
+              acc.z += wq * vq[k].z;
+              acc.w += wq * vq[k].w;
+            }
             M = Mn;
           }
-          sMrow[r] = M;
-          sLrow[r] = l;
-        }
-        __syncthreads();
-                const int dq = lane, rg = warp;
-        for (int r = rg; r < p.rows; r += W) {
-          const float M = sMrow[r];
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-          for (int q = 0; q < cnt; ++q) {
-            const size_t sl = slots[q];
-            const float wq = ex2(__ldcg(p.part_ml + sl * 2 * RP + r) - M);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                        p.part_o + (sl * RP + r) * kHeadDim) +
-                                    dq);
-            acc.x += wq * v.x;
-            acc.y += wq * v.y;
-            acc.z += wq * v.z;
-            acc.w += wq * v.w;
-          }
-          const float inv = sLrow[r] > 0.f ? v_mult / sLrow[r] : 0.f;
+          const float inv = l > 0.f ? v_mult / l : 0.f;
           const int i = r / p.group, gh = r % p.group;
           const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
           if constexpr (kPartial) {
             *reinterpret_cast<float4*>(p.out_o + orow * kHeadDim + 4 * dq) =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            if (dq == 0)
-              p.out_lse[orow] = sLrow[r] > 0.f ? (M + __log2f(sLrow[r])) * kLn2 : -INFINITY;
+            if (dq == 0) p.out_lse[orow] = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
           } else {
             __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
             __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
