@@ -98,10 +98,14 @@ struct AttnCfg {
   // for 24 and 32 rows too (8-bit formats), and two ring stages per warp for
   // 16 and 32 rows so its buffers and per-sequence array fit
   static constexpr bool kTree = NT <= 2 || (kWideTree && KVT != PQKV_KV_FP16);
+  // 8 query rows (not the sliding-window kernels): instead of the tree every
+  // warp writes its O to a buffer of its own, and after one barrier every
+  // thread adds one float4 of the output over the warps
+  static constexpr bool kFlat = NT == 1 && !kWideTree;
   static constexpr int kCombGroups = kW >= 12 ? kW / 4 : 1;
   static constexpr int kCombSize = kW / kCombGroups;
   static constexpr int kOBytes = kRP * kHeadDim * 4;     // one buffer
-  static constexpr int kOBuffers = kTree ? kW / 2 : kCombGroups;
+  static constexpr int kOBuffers = kFlat ? kW : (kTree ? kW / 2 : kCombGroups);
   static constexpr int kMLOff = kOOff + kOBuffers * kOBytes;
   static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
   static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
@@ -1164,6 +1168,22 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
           o[mt][nt][c + 2] *= fw;
         }
       }
+    if constexpr (Cfg::kFlat) {
+      // every warp's rescaled O to its own buffer (the lane's four float4
+      // slots of a row permuted by g / 2: conflict-free stores) ...
+      {
+        float4* dst = reinterpret_cast<float4*>(sO + (size_t)warp * RP * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            dst[((2 * t + c) * kHeadDim + 16 * g) / 4 + (k4 ^ (g >> 1))] =
+                make_float4(o[2 * k4][0][c], o[2 * k4][0][c + 2], o[2 * k4 + 1][0][c],
+                            o[2 * k4 + 1][0][c + 2]);
+      }
+      __syncthreads();
+    }
+    if constexpr (!Cfg::kFlat) {
 #pragma unroll 1
     for (int n = W; n > 1;) {
       const int half = (n + 1) >> 1;
@@ -1199,9 +1219,57 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
       n = half;
     }
 
+    }
     const int cnt = *frag_cnt;
     const int slot = sp.k > 0 ? (int)blockIdx.x : f_seg + (int)blockIdx.x;
     const int64_t out_row0 = (int64_t)f_s * p.q_len;
+    if constexpr (Cfg::kFlat) {
+      // ... then thread (r, dq) adds float4 dq of row r over the warps and
+      // writes the output or the partial
+      for (int it = tid; it < p.rows * 32; it += nthr) {
+        const int r = it >> 5, dq = it & 31;
+        const int sidx = r * 32 + (dq & ~3) + ((dq & 3) ^ (dq >> 3));
+        float M = sML[r];
+#pragma unroll
+        for (int w = 1; w < W; ++w) M = fmaxf(M, sML[(w * 2) * RP + r]);
+        float l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          l += ex2(sML[(w * 2) * RP + r] - M) * sML[(w * 2 + 1) * RP + r];
+          const float4 v = reinterpret_cast<const float4*>(sO + (size_t)w * RP * kHeadDim)[sidx];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        const int i = r / p.group, gh = r % p.group;
+        const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
+        if (cnt == 1) {
+          const float f = l > 0.f ? v_mult / l : 0.f;
+          if constexpr (kPartial) {
+            *reinterpret_cast<float4*>(p.out_o + orow * kHeadDim + 4 * dq) =
+                make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+            if (dq == 0) p.out_lse[orow] = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
+          } else {
+            __half2 h01 = __floats2half2_rn(acc.x * f, acc.y * f);
+            __half2 h23 = __floats2half2_rn(acc.z * f, acc.w * f);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+          }
+        } else {
+          *reinterpret_cast<float4*>(p.part_o + ((size_t)slot * RP + r) * kHeadDim + 4 * dq) = acc;
+          if (dq == 0) {
+            p.part_ml[(size_t)slot * 2 * RP + r] = M;
+            p.part_ml[(size_t)slot * 2 * RP + RP + r] = l;
+          }
+        }
+      }
+      // the buffers are read; the next fragment's warps may write them
+      __syncthreads();
+    } else {
     if (warp == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -1246,6 +1314,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
             }
           }
         }
+    }
     }
         if (cnt > 1) {
       // warp 0's partial writes, ordered by the barrier before thread 0's
