@@ -37,8 +37,12 @@
  *     array present on every GPU that loads the library, its per-device
  *     address cache and the last call's contents; see that entry point).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
- *     default stream).  The return value reports argument validation and
- *     launch errors only.
+ *     default stream), in stream order.  Most kernels are launched with
+ *     programmatic dependent launch allowed: their blocks may become resident
+ *     while the previous kernel on the stream finishes, but they wait for it
+ *     to complete (and its writes to be visible) before touching memory, so
+ *     the ordering is that of a plain launch.  The return value reports
+ *     argument validation and launch errors only.
  *   - Errors that only the device can see are OR-ed as PQKV_DEV_* bits into
  *     `*status` (a device int32, may be NULL).  The offending work is skipped;
  *     no kernel traps, asserts or waits without a bound.
