@@ -287,6 +287,15 @@ struct FragIterT {
       e = sp.start(c + 1);
     }
   }
+  // the same with the block's share [x0, x1) already known
+  __device__ void init_range(const SplitT<kCost>& split, int cta, int64_t x0, int64_t x1) {
+    sp = split;
+    c = cta;
+    s = 0;
+    fixed_done = false;
+    x = x0;
+    e = x1;
+  }
 
   __device__ bool next(Frag& f) {
     if (sp.k > 0) {
@@ -632,6 +641,48 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   }
   const int ntot = (int)(x1 - x0);
 
+  // Tree-combine kernels whose query rows take one vector per thread (8 and
+  // 16 rows): the query rows and scales of the block's first segment are read
+  // now, beside the first block-table lookups.
+  constexpr bool kEarlyQ = Cfg::kTree && RP * 16 <= nthr;
+  uint4 q_early = make_uint4(0, 0, 0, 0);
+  int early_seg = -1;
+  float ks0 = 1.f, vs0 = 1.f;
+  int qpos0 = 0;
+  if constexpr (kEarlyQ) {
+    if (ntot > 0) {
+      int s0 = 0, h0 = 0;
+      if (sp.k == 0) {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if ((int64_t)pre[mid] * H <= x0) lo = mid; else hi = mid - 1;
+        }
+        s0 = lo;
+        h0 = (int)((x0 - (int64_t)pre[lo] * H) / sp.pages(lo));
+      } else {
+        const int seg = blockIdx.x / sp.k;
+        s0 = seg / H;
+        h0 = seg % H;
+      }
+      early_seg = s0 * H + h0;
+      if constexpr (KVT != PQKV_KV_FP16 && KVT != PQKV_KV_INT8_ROW) {
+        const int sh = p.scale_per_head ? h0 : 0;
+        ks0 = __ldg(p.k_scale + sh);
+        vs0 = __ldg(p.v_scale + sh);
+      }
+      if constexpr (kPartial) qpos0 = p.q_pos[s0];
+      if (tid < RP * 16) {
+        const int r = tid >> 4, c8 = tid & 15;
+        if (r < p.rows) {
+          const int i = r / p.group, gh = r % p.group;
+          const int64_t row = ((int64_t)s0 * p.q_len + i) * p.num_q_heads + h0 * p.group + gh;
+          q_early = __ldg(reinterpret_cast<const uint4*>(p.q + row * kHeadDim) + c8);
+        }
+      }
+    }
+  }
+
   // -- tile feed: warp w streams the block's pages w, w+W, w+2W, ... into its
   //    own stages.  Its u-th page is i = w + u*W; lane l caches the kv-head
   //    and pool page of the warp's pages u in [ubase, ubase+32) (cur) and the
@@ -709,9 +760,15 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   };
 #pragma unroll 1
   for (int k = 0; k < SPW; ++k) issue_next();
+  if constexpr (kEarlyQ) {
+    if (early_seg >= 0 && tid < RP * 16) reinterpret_cast<uint4*>(sQ)[tid] = q_early;
+  }
 
   // -- walk the fragments of the block's range in lock step
-  if (tid == 0) sit->init(sp, blockIdx.x);
+  if (tid == 0) {
+    if constexpr (Cfg::kTree) sit->init_range(sp, blockIdx.x, x0, x1);
+    else sit->init(sp, blockIdx.x);
+  }
   uint32_t n0 = 0;
   int consumed_u = 0;
   int cur_seg = -1, cur_L = 0;
@@ -730,7 +787,26 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     // ---- (re)load the query rows of this (sequence, kv-head)
     if (f_seg != cur_seg) {
       const int L = slen[f_s];
-      for (int v = tid; v < RP * 16; v += nthr) {
+      // tree-combine kernels: the scales (and the partial mode's query
+      // position) are read beside the query rows, not after the barrier
+      float ks_e = 1.f, vs_e = 1.f;
+      int qpos_e = 0;
+      const bool q_read = kEarlyQ && f_seg == early_seg;
+      if constexpr (Cfg::kTree) {
+        if (q_read) {
+          ks_e = ks0;
+          vs_e = vs0;
+          qpos_e = qpos0;
+        } else {
+          if constexpr (KVT != PQKV_KV_FP16 && KVT != PQKV_KV_INT8_ROW) {
+            const int sh = p.scale_per_head ? f_h : 0;
+            ks_e = __ldg(p.k_scale + sh);
+            vs_e = __ldg(p.v_scale + sh);
+          }
+          if constexpr (kPartial) qpos_e = p.q_pos[f_s];
+        }
+      }
+      for (int v = tid; v < RP * 16 && !q_read; v += nthr) {
         const int r = v >> 4, c8 = v & 15;
         uint4 val = make_uint4(0, 0, 0, 0);
         if (r < p.rows) {
@@ -757,14 +833,15 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
         qk_scale = p.sm_scale_log2;
         v_mult = 1.f;
       } else {
-        const float ks = __ldg(p.k_scale + sh), vs = __ldg(p.v_scale + sh);
+        const float ks = Cfg::kTree ? ks_e : __ldg(p.k_scale + sh);
+        const float vs = Cfg::kTree ? vs_e : __ldg(p.v_scale + sh);
         if (!(ks > 0.f && ks <= 3.4e38f && vs > 0.f && vs <= 3.4e38f))
           report(p.status, PQKV_DEV_BAD_SCALE);
         qk_scale = ks * p.sm_scale_log2;
         v_mult = vs;
       }
       inv_qk_scale = 1.f / qk_scale;
-      if constexpr (kPartial) lim_min = p.q_pos[f_s];
+      if constexpr (kPartial) lim_min = Cfg::kTree ? qpos_e : p.q_pos[f_s];
       else lim_min = L - p.q_len;
       // causal limit per row: the last key position row r may see
       if constexpr (Cfg::kRowsInSmem) {
