@@ -87,10 +87,12 @@ struct AttnCfg {
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kRingOff = 0;
   static constexpr int kOOff = kRingOff + kStages * kTileBytes;
-  // Fragment-end combine of the warps' O.  8 and 16 query rows: a tree (in
-  // each round the upper half of the remaining warps hands its O to the lower
-  // half, kW / 2 buffers in the first round; warp 0 writes the result from
-  // registers).  24 and 32 rows: groups of four warps take turns on a group
+  // Fragment-end combine of the warps' O.  8 and 16 query rows (kTree): a
+  // tree (in each round the upper half of the remaining warps hands its O to
+  // the lower half, kW / 2 buffers in the first round; warp 0 writes the
+  // result from registers), or for 8 rows the flat combine below; these
+  // kernels also share the one-pass merge and the early fragment set-up.
+  // 24 and 32 rows: groups of four warps take turns on a group
   // buffer (8 warps: one group), then the group buffers are added in fixed
   // order -- the 24-row page loop compiled slower with the tree epilogue,
   // and the 32-row kernel has no shared memory left for its buffers.
@@ -1209,11 +1211,13 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     }
     } else {
     // ---- fragment end.  Every warp publishes its (m, l) per row; each warp
-    // rescales its O to the block's row maximum; a tree then adds the warps'
-    // O (in each round the upper half of the remaining warps hands its O to
-    // the lower half through shared memory), so warp 0 ends with the
-    // fragment's O in registers and writes the output or the partial from
-    // there.  Fixed order throughout, so the result is deterministic.
+    // rescales its O to the block's row maximum; then either the flat
+    // combine (kFlat: every warp's O to its own buffer, every thread adds one
+    // float4 over the warps and writes it) or a tree adds the warps' O (in
+    // each round the upper half of the remaining warps hands its O to the
+    // lower half through shared memory, so warp 0 ends with the fragment's O
+    // in registers and writes the output or the partial from there).  Fixed
+    // order throughout, so the result is deterministic.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
