@@ -781,6 +781,16 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   int lim_min = 0;
   bool dead = false;
 
+  // Launched as a cluster (one segment split over at most 8 blocks; the FP16
+  // 8-row kernel only, the others have no registers to spare for it): each
+  // block leaves its combined O, m and l in its idle ring, and
+  // block 0 of the cluster merges them through distributed shared memory at
+  // the end, instead of global partials and a ticket.
+  constexpr bool kClusterMerge = Cfg::kFlat && !kPair && !kWin && KVT == PQKV_KV_FP16;
+  uint32_t ncl = 1;
+  if constexpr (kClusterMerge) ncl = cluster_nctarank();
+  const bool clu = kClusterMerge && ncl > 1;
+  bool clu_written = false;
   for (;;) {
     if (tid == 0) *has_frag = sit->next(*sf) ? 1 : 0;
     __syncthreads();
@@ -1313,7 +1323,12 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     const int64_t out_row0 = (int64_t)f_s * p.q_len;
     if constexpr (Cfg::kFlat) {
       // ... then thread (r, dq) adds float4 dq of row r over the warps and
-      // writes the output or the partial
+      // writes the output or the partial.  Launched as a cluster (one
+      // segment split over the cluster's blocks), each block keeps its result
+      // in its (now idle) ring and block 0 merges them through distributed
+      // shared memory, instead of global partials and a ticket.
+      float4* cP = reinterpret_cast<float4*>(ring);
+      float* cML = reinterpret_cast<float*>(ring + RP * kHeadDim * 4);
       for (int it = tid; it < p.rows * 32; it += nthr) {
         const int r = it >> 5, dq = it & 31;
         const int sidx = r * 32 + (dq & ~3) + ((dq & 3) ^ (dq >> 3));
@@ -1330,6 +1345,15 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
           acc.y += v.y;
           acc.z += v.z;
           acc.w += v.w;
+        }
+        if (clu) {
+          cP[r * 32 + dq] = acc;
+          if (dq == 0) {
+            cML[r] = M;
+            cML[RP + r] = l;
+          }
+          clu_written = true;
+          continue;
         }
         const int i = r / p.group, gh = r % p.group;
         const int64_t orow = (out_row0 + i) * p.num_q_heads + f_h * p.group + gh;
@@ -1404,7 +1428,7 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
         }
     }
     }
-        if (cnt > 1) {
+        if (cnt > 1 && !clu) {
       // warp 0's partial writes, ordered by the barrier before thread 0's
       // release; the last block's acquire, then the barrier, orders its
       // partial loads after every other block's release
@@ -1500,6 +1524,65 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     }
     }
     __syncthreads();
+  }
+
+  if constexpr (kClusterMerge) {
+    if (clu) {
+      // a block whose share was empty leaves a neutral partial; every block
+      // arrives at both cluster barriers exactly once
+      float4* cP = reinterpret_cast<float4*>(ring);
+      float* cML = reinterpret_cast<float*>(ring + RP * kHeadDim * 4);
+      if (!__syncthreads_or(clu_written)) {
+        for (int it = tid; it < p.rows * 32; it += nthr) {
+          const int r = it >> 5, dq = it & 31;
+          cP[r * 32 + dq] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (dq == 0) {
+            cML[r] = kNoScore;
+            cML[RP + r] = 0.f;
+          }
+        }
+      }
+      __syncthreads();
+      cluster_sync_all();
+      if (cluster_ctarank() == 0) {
+        // the cluster's one segment: sequence 0, kv-head 0; 8-warp flat
+        // kernels are FP16, so no V scale
+        for (int it = tid; it < p.rows * 32; it += nthr) {
+          const int r = it >> 5, dq = it & 31;
+          float M = kNoScore;
+          for (uint32_t c = 0; c < ncl; ++c)
+            M = fmaxf(M, ld_cluster_f32(cluster_map(smem_u32(cML + r), c)));
+          float l = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (uint32_t c = 0; c < ncl; ++c) {
+            const float w = ex2(ld_cluster_f32(cluster_map(smem_u32(cML + r), c)) - M);
+            l += w * ld_cluster_f32(cluster_map(smem_u32(cML + RP + r), c));
+            const float4 v = ld_cluster_f4(cluster_map(smem_u32(cP + r * 32 + dq), c));
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+          }
+          const float f = l > 0.f ? 1.f / l : 0.f;
+          const int i = r / p.group, gh = r % p.group;
+          const int64_t orow = (int64_t)i * p.num_q_heads + gh;
+          if constexpr (kPartial) {
+            *reinterpret_cast<float4*>(p.out_o + orow * kHeadDim + 4 * dq) =
+                make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+            if (dq == 0) p.out_lse[orow] = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
+          } else {
+            __half2 h01 = __floats2half2_rn(acc.x * f, acc.y * f);
+            __half2 h23 = __floats2half2_rn(acc.z * f, acc.w * f);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * dq) = pk;
+          }
+        }
+      }
+      // every block's shared memory stays until block 0 has read it
+      cluster_sync_all();
+    }
   }
 
   // ---- drain: never leave with a tile copy in flight (only after a timeout

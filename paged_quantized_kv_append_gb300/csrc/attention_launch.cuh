@@ -31,6 +31,13 @@ cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& map, int 
   const cudaError_t e = opt_in_smem(paged_attention_kernel<KVT, NT, AttnParams, kPair>,
                                     Cfg::smem_bytes(PQKV_MAX_SEQS), attr_done);
   if (e != cudaSuccess) return e;
+  if constexpr (Cfg::kFlat && !kPair && KVT == PQKV_KV_FP16) {
+    // one segment over at most 8 blocks: a cluster, merged in shared memory
+    if (p.num_splits == 0 && p.num_seqs * p.num_kv_heads == 1 && grid > 1 && grid <= 8)
+      return launch_cluster(paged_attention_kernel<KVT, NT, AttnParams, kPair>, grid,
+                            Cfg::kThreads, Cfg::smem_bytes(p.num_seqs), stream, (unsigned)grid,
+                            attention_uses_pdl<KVT, NT, AttnParams, kPair>(), map, p);
+  }
   if constexpr (attention_uses_pdl<KVT, NT, AttnParams, kPair>()) {
     return launch_pdl(paged_attention_kernel<KVT, NT, AttnParams, kPair>, grid, Cfg::kThreads,
                       Cfg::smem_bytes(p.num_seqs), stream, map, p);

@@ -280,3 +280,20 @@ def test_maximum_sequence_count():
         o = out.float().cpu().numpy().reshape(8, 256 * 5, 32, 128)
         for copy in range(8):
             assert_close(o[copy], ref, "2048 sequences copy %d splits=%d" % (copy, ns))
+
+
+@pytest.mark.parametrize("L", [1, 7, 16, 100, 513, 1024])
+@pytest.mark.parametrize("hint", ["none", "exact"])
+def test_one_segment_fp16_decode_with_empty_shares(L, hint):
+    """One sequence on one kv-head, FP16, 8 query rows: a split over up to 8
+    blocks is launched as a thread-block cluster whose blocks merge in shared
+    memory.  The block table has room for 1024 tokens, so without a length
+    hint the grid is sized for 1024 and, for short sequences, some blocks
+    (block 0 too, for L = 1) get empty shares; they must still take part in
+    the merge."""
+    w = W.Workload("one_segment", 90 + L, [L], 8, 1, 1, W.FP16, outliers=False, pool_slack=0.5)
+    c = Case(w)
+    bt = torch.full((1, 64), -1, dtype=torch.int32, device="cuda")
+    bt[:, :c.bt.shape[1]] = c.bt
+    out = c.attention(bt=bt, max_seq_len=(L if hint == "exact" else 0))
+    assert_close(out, c.oracle_attention(), "L %d hint %s" % (L, hint))
