@@ -125,7 +125,9 @@ class ClockSampler:
     def summarize(cls, path, t_start, t_end):
         import datetime as dt
         sm, smax, reasons, total = [], None, set(), 0
-        for line in open(path):
+        with open(path) as f:
+            lines = f.readlines()
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 10:
                 continue

@@ -12,6 +12,11 @@ from paged_quantized_kv_append_gb300 import build as pqbuild
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pqkv.h")
 
+
+def _header_text():
+    with open(HEADER) as f:
+        return f.read()
+
 OK, EINVAL, EUNSUPPORTED, ERANGE, EWORKSPACE, ECUDA = 0, -1, -2, -3, -4, -5
 
 
@@ -22,7 +27,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = _header_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pqkv_\w+)\s*\(", text)) - {"PQKV_COUNTER_BYTES"})
 
@@ -34,7 +39,7 @@ def test_header_declares_the_entry_points():
 
 
 def test_header_and_binding_agree_on_formats():
-    text = open(HEADER).read()
+    text = _header_text()
     for name, code in (("PQKV_KV_FP16", 0), ("PQKV_KV_FP8_E4M3", 1), ("PQKV_KV_INT8", 2),
                        ("PQKV_KV_INT8_ROW", 3)):
         assert re.search(r"\b%s = %d\b" % (name, code), text), name
@@ -169,7 +174,7 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
 
 def _declared_params():
     """{function: number of parameters} from the header's prototypes."""
-    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"/\*.*?\*/", "", _header_text(), flags=re.S)
     text = re.sub(r"#define[^\n]*", "", text)
     out = {}
     for m in re.finditer(r"\b(pqkv_\w+)\s*\(([^;{]*?)\)\s*;", text):

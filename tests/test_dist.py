@@ -36,9 +36,9 @@ def _rank_main(rank, world, port, out):
 def test_max_over_ranks_world2_gloo():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
-    out = mgr.dict()
     ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
     procs = [ctx.Process(target=_rank_main, args=(r, world, port, out)) for r in range(world)]
     for p in procs:
         p.start()
@@ -106,9 +106,9 @@ def _dcp_rank(rank, world, port, out):
 def test_dcp_split_over_two_gloo_ranks_equals_full_attention():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
-    out = mgr.dict()
     ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
     procs = [ctx.Process(target=_dcp_rank, args=(r, world, port, out)) for r in range(world)]
     for p in procs:
         p.start()

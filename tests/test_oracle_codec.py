@@ -20,7 +20,9 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ofp8_e4m3_special_va
 
 def _golden_rows():
     rows = []
-    for line in open(GOLDEN):
+    with open(GOLDEN) as f:
+        lines = f.readlines()
+    for line in lines:
         line = line.strip()
         if not line or line.startswith("#"):
             continue
