@@ -116,3 +116,28 @@ def test_captured_int8_decode_step_appends_and_attends():
         assert np.array_equal(pages.cpu().numpy(), pool), "replay %d: pool differs" % i
         assert_close(out, ref, "int8 decode replay %d" % i)
     assert int(status.item()) == 0
+
+
+def test_captured_one_segment_fp16_decode_replays_like_the_oracle():
+    """The tiny FP16 decode (one segment over 8 blocks, launched as a
+    thread-block cluster that merges in shared memory) captured in a graph:
+    several replays, each equal to the eager launch and within tolerance of
+    the oracle."""
+    pq = require_gpu()
+    c = Case(W.workload("tiny_fp16_decode"))
+    w = c.w
+    ref = c.oracle_attention()
+    eager = c.attention()
+    out = torch.full_like(c.q, float("nan"))
+
+    def step():
+        pq.paged_attention(c.q, c.pages, c.bt, c.seq_lens, w.q_len, w.kv_dtype, c.ks, c.vs, out,
+                           max_seq_len=max(w.seq_lens))
+
+    g = _capture(step)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+        assert_close(out, ref, "tiny decode, graph replay")
