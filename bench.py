@@ -46,6 +46,10 @@ def parse_args():
     ap.add_argument("--scale", type=float, default=1.0,
                     help="context-length scale of the workload (1.0 = the full workload; "
                          "smaller values are for profiling captures)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window of keys per query (0: none); the attention reads "
+                         "only the pages some query's window holds, and its algorithmic bytes "
+                         "count those")
     ap.add_argument("--append-tokens", type=int, default=0,
                     help="size of the step's append chunk for workloads that have one "
                          "(default: the workload's own; e.g. 8192 with --scale 0.25 profiles "
@@ -234,15 +238,19 @@ def kernel_source_hash(texts=None):
     return h.hexdigest()[:16]
 
 
-def measured_traffic():
+def measured_traffic(workload, full_size):
     """DRAM bytes per attention launch from a committed ncu summary, if it was
-    taken on the current kernel source; otherwise None."""
+    taken on the current kernel source and on this line's configuration (the
+    workload at full size, balanced split, no window); otherwise None."""
     p = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
     try:
-        d = json.load(open(p))
+        with open(p) as f:
+            d = json.load(f)
     except (OSError, ValueError):
         return None
     if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    if d.get("workload") != workload or not full_size:
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -648,6 +656,8 @@ def run_pqkv(args, rank, local, world):
     w = ctx["w"]
     stream = torch.cuda.current_stream()
     attn_bytes, app_bytes = algorithmic_bytes(ctx)
+    if args.window:
+        attn_bytes = window_bytes(w, args.window)
     appends = "ak" in ctx
     launches_per_step = 1 + (1 if appends else 0)
 
@@ -660,7 +670,7 @@ def run_pqkv(args, rank, local, world):
         pq.paged_attention(ctx["q"], ctx["pages"], ctx["bt"], ctx["seq_lens"], w.q_len,
                            w.kv_dtype, ctx["ks"], ctx["vs"], ctx["out"],
                            num_splits=args.num_splits, workspace=ctx["ws"],
-                           max_seq_len=max(w.seq_lens))
+                           max_seq_len=max(w.seq_lens), window=args.window)
         if ev is not None:
             ev[1].record(stream)
 
@@ -763,7 +773,8 @@ def run_pqkv(args, rank, local, world):
                                    ctx["vs"], ctx["pages"])
             pq.paged_attention(d["q"], ctx["pages"], d["bt"], d["seq_lens"], w.q_len, w.kv_dtype,
                                ctx["ks"], ctx["vs"], outs[b], num_splits=args.num_splits,
-                               workspace=ctx["ws"], max_seq_len=max(w.seq_lens))
+                               workspace=ctx["ws"], max_seq_len=max(w.seq_lens),
+                               window=args.window)
             ev_freed[b].record(stream)
             out_host[b].copy_(outs[b], non_blocking=True)
             ev_done[b].record(stream)
@@ -796,7 +807,8 @@ def run_pqkv(args, rank, local, world):
 
     peak, peak_src = hbm_peak()
     configs = None
-    if not args.no_per_config and args.scale == 1.0 and args.workload == "e4m3_verify_512k_stress":
+    if (not args.no_per_config and args.scale == 1.0 and not args.window and
+            args.workload == "e4m3_verify_512k_stress"):
         configs = per_config(pq, W, dev, peak, ctx, attn_avg * 1e3)
     clocks.close()
     clk = clocks.window(load_start, load_end)
@@ -824,13 +836,16 @@ def run_pqkv(args, rank, local, world):
                    else w.seq_lens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "page_size": w.page_size, "q_len": w.q_len,
                    "append_tokens": W.step_append_tokens(w), "num_splits": args.num_splits,
+                   "window": args.window,
                    "attention_bytes": attn_bytes, "append_bytes": app_bytes,
                    "l2": "inputs larger than L2 (%.2f GB of KV per step)" % (w.kv_bytes() / 1e9)},
         "roofline": {"bound": "hbm", "kernel": "paged_attention_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src
                      if peak_src == "measured" else "fallback",
-                     "traffic": measured_traffic(), "attention_us": attn_avg * 1e3},
+                     "traffic": measured_traffic(w.name, args.scale == 1.0 and not args.window and
+                                                 args.num_splits == 0),
+                     "attention_us": attn_avg * 1e3},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
