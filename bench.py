@@ -581,14 +581,16 @@ def append_entry(pq, W, device, peak, ks, vs, n_sets=6):
 
 
 def per_config(pq, W, device, peak, headline_ctx, headline_us):
-    """Every workload of the path at full size, plus the 8192-token append."""
+    """Every workload of the path at full size (with the row-scaled INT8 and
+    32-row verify variants), plus the 8192-token append."""
     import gc
     import torch
     out = {}
     flush = L2Flush(device)
     out[headline_ctx["w"].name] = config_entry(pq, W, headline_ctx, peak, headline=headline_us)
     for name in ("tiny_fp16_decode", "e4m3_decode_b8", "e4m3_verify_131k",
-                 "int8_decode_append_262k"):
+                 "int8_decode_append_262k", "int8_row_decode_262k", "int8_row_verify_131k",
+                 "e4m3_verify_q8_131k"):
         ctx = setup(name, device)
         small = ctx["w"].kv_bytes() < 2 * flush.l2
         out[name] = config_entry(pq, W, ctx, peak, flush=flush if small else None)

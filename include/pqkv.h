@@ -25,9 +25,11 @@
  * streams.
  * PQKV_KV_INT8_ROW pools carry a scale area right after the codes, in the same
  * allocation (num_pages*num_kv_heads*4096 bytes from the start of `pages`):
- *   float row_scale[num_pages][num_kv_heads][2][page_size]
- * (index 0 of the third axis: K rows, 1: V rows), i.e. 128 bytes per
- * (page, kv-head); the allocation is num_pages*num_kv_heads*4224 bytes.
+ *   fp16 row_scale[num_pages][num_kv_heads][8][4]
+ * (IEEE binary16), where [p][h][i] holds the scales of K row i, K row i+8,
+ * V row i and V row i+8 of page p, kv-head h -- the order in which the
+ * attention kernel's matrix fragments consume them.  That is 64 bytes per
+ * (page, kv-head); the allocation is num_pages*num_kv_heads*4160 bytes.
  *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers owned by the caller.  Nothing
@@ -112,11 +114,12 @@ enum {
  *     INT8: round half to even, clamp to [-127, 127] (NaN -> 0);
  *     FP16: the fp16 bits unchanged (scales ignored, may be NULL).
  * INT8_ROW: for each written (token, kv-head) row x of K (and of V) the row's
- * scale r = fp32(amax / 127), amax = the largest |x_d| of the row (NaNs
- * ignored; 0 for a row of zeros), correctly rounded, is stored in the scale
- * area at the row's slot and the codes are the INT8 codes of fp32(x_d) / r
- * (a zero r gives 0/0 = NaN -> code 0).  k_scale / v_scale are ignored (may
- * be NULL).  V rows with amax above 32512 exceed what the attention kernel's
+ * scale r = fp16(amax / 127), the binary16 value nearest the exact quotient
+ * (ties to even), amax = the largest |x_d| of the row (NaNs ignored; 0 for a
+ * row of zeros), is stored in the scale area at the row's slot and the codes
+ * are the INT8 codes of fp32(x_d) / fp32(r).  A zero r (amax <= 127 * 2^-25)
+ * gives 0/0 = NaN -> code 0 and +-x/0 -> +-127, all worth 0.  k_scale /
+ * v_scale are ignored (may be NULL).  V rows with amax above 32512 exceed what the attention kernel's
  * fp16 products hold (probability <= 256 times the row scale).
  *
  *   k, v            fp16 [num_tokens][num_kv_heads][head_dim]; heads and dims

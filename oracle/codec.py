@@ -104,12 +104,14 @@ def scaled_input(x16, scale) -> np.ndarray:
 
 
 def int8_row_scale(x16) -> np.ndarray:
-    """binary32 scale of each row (last axis) of fp16 values for format 3:
-    fp32(amax / 127), amax = the row's largest |x| with NaNs ignored (0 when
-    nothing else is left).  The quotient of two exact values is rounded once."""
+    """Scale of each row (last axis) of fp16 values for format 3, a binary16
+    value (returned as float32, which holds it exactly): fp16(amax / 127),
+    amax = the row's largest |x| with NaNs ignored (0 when nothing else is
+    left).  The quotient is formed in float64 and rounded once more to fp16;
+    double rounding is innocuous for division since 53 >= 2*11 + 2."""
     a = np.abs(np.asarray(x16, dtype=np.float16).astype(np.float64))
     a = np.where(np.isnan(a), 0.0, a)
-    return (a.max(axis=-1) / INT8_MAX).astype(np.float32)
+    return (a.max(axis=-1) / INT8_MAX).astype(np.float16).astype(np.float32)
 
 
 def quantize(x16, scale, kv_dtype: int) -> np.ndarray:

@@ -133,7 +133,7 @@ def _dtype_id(kv_dtype) -> int:
 
 
 def _row_scale_bytes(num_pages, num_kv_heads):
-    return num_pages * num_kv_heads * 2 * PAGE_SIZE * 4
+    return num_pages * num_kv_heads * 2 * PAGE_SIZE * 2          # fp16 scales
 
 
 def new_pages(num_pages: int, num_kv_heads: int, kv_dtype, device="cuda", fill=None):
@@ -158,15 +158,17 @@ def new_pages(num_pages: int, num_kv_heads: int, kv_dtype, device="cuda", fill=N
 
 
 def row_scales(pages: torch.Tensor) -> torch.Tensor:
-    """float32 [num_pages, Hkv, 2, 16] view of an INT8_ROW pool's row scales
-    (index 0 of the third axis: K rows, 1: V rows)."""
+    """float16 view [num_pages, Hkv, 2, 2, 8] of an INT8_ROW pool's row scales:
+    ``[p, h, kv, r // 8, r % 8]`` is the scale of row r (slot 16 p + r) of K
+    (kv 0) or V (kv 1).  The area stores them as [p][h][r % 8][kv][r // 8];
+    ``.reshape(n, Hkv, 2, 16)`` gives a row-ordered copy."""
     _check_pages(pages, INT8_ROW)
     n, H = pages.shape[0], pages.shape[1]
     codes = pages.numel()
     whole = torch.empty(0, dtype=torch.uint8, device=pages.device)
     whole.set_(pages.untyped_storage(), pages.storage_offset(),
                (codes + _row_scale_bytes(n, H),))
-    return whole[codes:].view(torch.float32).view(n, H, 2, PAGE_SIZE)
+    return whole[codes:].view(torch.float16).view(n, H, 8, 2, 2).permute(0, 1, 3, 4, 2)
 
 
 def _check_pages(pages, kd):

@@ -72,8 +72,8 @@ bool uses_scale_args(int kv_dtype) {
 }
 
 // INT8_ROW: the row scales follow the codes in the pool allocation
-float* row_scale_area(void* pages, int64_t num_pages, int32_t num_kv_heads) {
-  return reinterpret_cast<float*>(static_cast<uint8_t*>(pages) +
+uint16_t* row_scale_area(void* pages, int64_t num_pages, int32_t num_kv_heads) {
+  return reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(pages) +
                                   num_pages * num_kv_heads * 2 * kPageSize * kHeadDim);
 }
 
@@ -281,7 +281,8 @@ int bind_attention(const AttnArgs& a, const AttnLaunch& L, void* workspace,
   p.seq_lens = a.seq_lens;
   // INT8_ROW reads no scale arguments: its k_scale slot carries the row-scale area
   p.k_scale = a.kv_dtype == PQKV_KV_INT8_ROW
-                  ? row_scale_area(const_cast<void*>(a.pages), a.num_pages, a.num_kv_heads)
+                  ? reinterpret_cast<const float*>(
+                        row_scale_area(const_cast<void*>(a.pages), a.num_pages, a.num_kv_heads))
                   : a.k_scale;
   p.v_scale = a.v_scale;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -283,16 +283,23 @@ __global__ void __launch_bounds__(kAppendThreads, KVT == PQKV_KV_INT8_ROW ? 1 : 
         reinterpret_cast<uint4*>(vd)[1] = v1[u];
       } else if (KVT == PQKV_KV_INT8_ROW) {
         // all eight threads of the row reach this point together
-        const float kscale = __fdiv_rn(row_max8(amax16(k0[u], k1[u])), 127.f);
-        const float vscale = __fdiv_rn(row_max8(amax16(v0[u], v1[u])), 127.f);
+        // the row scale is the binary16 nearest to amax / 127 (rounding the
+        // binary32 quotient once more is exact: 24 >= 2 * 11 + 2)
+        const __half kh = __float2half_rn(__fdiv_rn(row_max8(amax16(k0[u], k1[u])), 127.f));
+        const __half vh = __float2half_rn(__fdiv_rn(row_max8(amax16(v0[u], v1[u])), 127.f));
+        const float kscale = __half2float(kh);
+        const float vscale = __half2float(vh);
         *reinterpret_cast<uint4*>(kd) =
             quantize16<PQKV_KV_INT8>(k0[u], k1[u], kscale, recip_of(kscale));
         *reinterpret_cast<uint4*>(vd) =
             quantize16<PQKV_KV_INT8>(v0[u], v1[u], vscale, recip_of(vscale));
         if (c[u] == 0) {
-          float* rs = p.row_scales + (page * p.num_kv_heads + h[u]) * 2 * kPageSize + off;
-          rs[0] = kscale;
-          rs[kPageSize] = vscale;
+          // the (page, kv-head)'s 32 scales are ordered for the attention
+          // kernel's fragments: [i][K row i, K row i+8, V row i, V row i+8]
+          uint16_t* rs = p.row_scales + (page * p.num_kv_heads + h[u]) * 2 * kPageSize +
+                         (off & 7) * 4 + (off >> 3);
+          rs[0] = __half_as_ushort(kh);
+          rs[2] = __half_as_ushort(vh);
         }
       } else {
         const int sh = p.scale_per_head ? h[u] : 0;

@@ -116,10 +116,10 @@ struct AttnCfg {
   static constexpr int kMLOff = kOOff + kOBuffers * kOBytes;
   static constexpr int kQOff = kMLOff + kW * 2 * kRP * 4;
   static constexpr int kQfOff = kQOff + kRP * kHeadDim * 2;
-  // INT8_ROW: the 32 row scales (16 K, 16 V) of each stage's (page, kv-head)
+  // INT8_ROW: the 32 fp16 row scales (16 K, 16 V) of each stage's (page, kv-head)
   static constexpr bool kRowScaled = (KVT == PQKV_KV_INT8_ROW);
   static constexpr int kScOff = kQfOff + kQfBytes;
-  static constexpr int kScBytes = kRowScaled ? kStages * 128 : 0;
+  static constexpr int kScBytes = kRowScaled ? kStages * 64 : 0;
   static constexpr int kBarOff = kScOff + kScBytes;
   static constexpr int kMiscOff = kBarOff + kStages * 8;
   // 32 query rows (NT 4) are short of registers: there the per-row causal
@@ -690,6 +690,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
   //    and pool page of the warp's pages u in [ubase, ubase+32) (cur) and the
   //    next 32 (nxt).
   const uint64_t policy = l2_evict_first_policy();
+  // INT8_ROW: two kv-heads' row scales share a 128-byte line and are read by
+  // different blocks at about the same time; they stay in L2 for the second
+  uint64_t scale_policy = policy;
+  if constexpr (Cfg::kRowScaled) scale_policy = l2_evict_last_policy();
   if (tid == 0) prefetch_tensormap(&map);
   auto lookup = [&](int u, int& id, int& h) {
     const int i = warp + u * W;
@@ -739,20 +743,22 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
     if (lane == 0) {
       const int stage = i % S;
       if constexpr (Cfg::kRowScaled) {
-        // the page's 32 row scales travel with its tile (one bulk copy on the
-        // same barrier); a page id outside the pool (reported, its codes read
-        // as zeros) gets zero scales, written before the barrier is armed
-        float* dst = reinterpret_cast<float*>(smem + Cfg::kScOff) + stage * 32;
+        // the page's 32 fp16 row scales travel with its tile (one bulk copy on
+        // the same barrier); a page id outside the pool (reported, its codes
+        // read as zeros) gets zero scales, written before the barrier is armed
+        uint16_t* dst = reinterpret_cast<uint16_t*>(smem + Cfg::kScOff) + stage * 32;
         const bool id_ok = id >= 0 && (int64_t)id < p.num_pages;
         if (!id_ok) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) reinterpret_cast<float4*>(dst)[k] = make_float4(0, 0, 0, 0);
+          for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(dst)[k] = make_uint4(0, 0, 0, 0);
         }
-        mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes + (id_ok ? 128 : 0));
+        mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes + (id_ok ? 64 : 0));
         tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, h, id, policy);
         if (id_ok)
-          bulk_load(dst, p.k_scale + ((int64_t)id * p.num_kv_heads + h) * 32, 128,
-                    &full[stage], policy);
+          bulk_load(dst,
+                    reinterpret_cast<const uint16_t*>(p.k_scale) +
+                        ((int64_t)id * p.num_kv_heads + h) * 32,
+                    64, &full[stage], scale_policy);
       } else {
         mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
         tma_load_4d(ring + stage * Cfg::kTileBytes, &map, &full[stage], 0, 0, h, id, policy);
@@ -921,8 +927,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
       page_qk<KVT, NT>(T, g, t, lane, qf, sc);
       if constexpr (Cfg::kRowScaled) {
         // INT8_ROW: scores of token g and token g+8 times their K row scales
-        const float* rs = reinterpret_cast<const float*>(smem + Cfg::kScOff) + stage * 32;
-        const float ks_g = rs[g], ks_g8 = rs[g + 8];
+        // (the stage's scales are [i][K row i, K row i+8, V row i, V row i+8])
+        const float2 ks = __half22float2(
+            *reinterpret_cast<const __half2*>(smem + Cfg::kScOff + stage * 64 + g * 8));
+        const float ks_g = ks.x, ks_g8 = ks.y;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           sc[nt][0] *= ks_g;
@@ -1007,9 +1015,10 @@ __global__ void __launch_bounds__(AttnCfg<KVT, NT, kPair>::kThreads,
           // O accumulates p_j * vscale_j * vcode_j; the row sums keep p_j
           // alone.  Tokens past the sequence end may hold stale scales, and
           // their probability 0 must not meet a NaN.
-          const float* rs = reinterpret_cast<const float*>(smem + Cfg::kScOff) + stage * 32;
-          const float vs_g = pos0 + g < cur_L ? rs[16 + g] : 0.f;
-          const float vs_g8 = pos0 + g + 8 < cur_L ? rs[24 + g] : 0.f;
+          const float2 vs = __half22float2(
+              *reinterpret_cast<const __half2*>(smem + Cfg::kScOff + stage * 64 + g * 8 + 4));
+          const float vs_g = pos0 + g < cur_L ? vs.x : 0.f;
+          const float vs_g8 = pos0 + g + 8 < cur_L ? vs.y : 0.f;
           pb[nt][0] = movmatrix_trans(pack_half2(pr[0] * vs_g, pr[1] * vs_g));
           pb[nt][1] = movmatrix_trans(pack_half2(pr[2] * vs_g8, pr[3] * vs_g8));
         } else {

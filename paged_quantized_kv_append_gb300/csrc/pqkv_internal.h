@@ -27,7 +27,7 @@ struct AppendParams {
   int32_t num_kv_heads;
   uint8_t* pages;
   int64_t num_pages;
-  float* row_scales;        // INT8_ROW: [num_pages][Hkv][2][16] after the codes
+  uint16_t* row_scales;     // INT8_ROW: fp16 bits [num_pages][Hkv][8][4] after the codes
   int32_t* status;
 };
 
@@ -36,7 +36,7 @@ struct AttnParams {
   uint16_t* out;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  const float* k_scale;     // INT8_ROW: the row scales [num_pages][Hkv][2][16]
+  const float* k_scale;     // INT8_ROW: the fp16 row scales [num_pages][Hkv][8][4]
   const float* v_scale;
   int32_t* counters;        // [B*Hkv] merge tickets (workspace)
   float* part_o;            // [slots][RP][128] unnormalised partial outputs

@@ -166,11 +166,12 @@ def test_every_int8_code_in_k_and_v(kv_dtype, q_len):
     else:
         pages = pq.new_pages(num_pages, 1, W.INT8_ROW, "cuda", fill=0)
         pages.copy_(torch.from_numpy(pool))
-        kp = rng.uniform(0.02, 0.08, (num_pages, 1, 16)).astype(np.float32)
-        vp = rng.uniform(0.01, 0.05, (num_pages, 1, 16)).astype(np.float32)
+        kp = rng.uniform(0.02, 0.08, (num_pages, 1, 16)).astype(np.float16)
+        vp = rng.uniform(0.01, 0.05, (num_pages, 1, 16)).astype(np.float16)
         sc = pq.row_scales(pages)
-        sc[:, :, 0].copy_(torch.from_numpy(kp))
-        sc[:, :, 1].copy_(torch.from_numpy(vp))
+        sc[:, :, 0].copy_(torch.from_numpy(kp).view(num_pages, 1, 2, 8))
+        sc[:, :, 1].copy_(torch.from_numpy(vp).view(num_pages, 1, 2, 8))
+        kp, vp = kp.astype(np.float32), vp.astype(np.float32)
         pq.paged_attention(q, pages, bt, sl, q_len, kv_dtype, None, None, out)
         ref = oracle.paged_attention(q.cpu().numpy(), pool, bt.cpu().numpy(), [L], q_len,
                                      kv_dtype, kp, vp)

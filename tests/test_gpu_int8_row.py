@@ -28,7 +28,7 @@ def _append_both(kvals, vvals, H, slots, num_pages, k_stride=None):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     pq.kv_append_quant(k, v, sl, T3, None, None, pages, status=status)
     got_codes = pages.cpu().numpy()
-    got_scales = pq.row_scales(pages).cpu().numpy()
+    got_scales = pq.row_scales(pages).reshape(num_pages, H, 2, 16).cpu().numpy()
     pool = oracle.new_pool(num_pages, H, 128, T3, fill=0x5A)
     kp = np.full((num_pages, H, 16), np.nan, np.float32)
     vp = np.full((num_pages, H, 16), np.nan, np.float32)
@@ -38,14 +38,22 @@ def _append_both(kvals, vvals, H, slots, num_pages, k_stride=None):
     return got_codes, got_scales, ref_codes, kp, vp
 
 
+def _fp16_bits(ref):
+    """binary16 bits of the oracle's float32 scales, which hold binary16 values"""
+    h = ref.astype(np.float16)
+    ok = ~np.isnan(ref)
+    assert np.array_equal(h[ok].astype(np.float32), ref[ok])
+    return h.view(np.uint16)
+
+
 def _same_scales(got, kp, vp):
     # bit-identical, NaN where nothing was written
+    assert got.dtype == np.float16
     for gi, ref in ((0, kp), (1, vp)):
-        a = got[:, :, gi].view(np.uint32)
-        b = ref.view(np.uint32)
+        a = got[:, :, gi].view(np.uint16)
         assert np.array_equal(np.isnan(got[:, :, gi]), np.isnan(ref))
         ok = ~np.isnan(ref)
-        assert np.array_equal(a[ok], b[ok])
+        assert np.array_equal(a[ok], _fp16_bits(ref)[ok])
 
 
 def test_every_fp16_value_in_rows_bit_exact():
@@ -94,10 +102,11 @@ def test_workload_pools_and_scales_bit_exact(name):
     pq = require_gpu()
     c = case(name)
     assert np.array_equal(c.gpu_pool_bytes(), c.pool_o)
-    got = pq.row_scales(c.pages).cpu().numpy()
+    n, H = c.pages.shape[:2]
+    got = pq.row_scales(c.pages).reshape(n, H, 2, 16).cpu().numpy()
     written = c.oracle_ks != 0                       # the oracle's pool starts at 0 like new_pages
-    assert np.array_equal(got[:, :, 0].view(np.uint32), c.oracle_ks.view(np.uint32))
-    assert np.array_equal(got[:, :, 1].view(np.uint32), c.oracle_vs.view(np.uint32))
+    assert np.array_equal(got[:, :, 0].view(np.uint16), _fp16_bits(c.oracle_ks))
+    assert np.array_equal(got[:, :, 1].view(np.uint16), _fp16_bits(c.oracle_vs))
     assert written.any()
 
 

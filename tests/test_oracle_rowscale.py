@@ -2,7 +2,7 @@
 
 Pinned against things outside the oracle's own formula: the INT8 codec with
 one scale (itself pinned in test_oracle_codec.py), exact rational arithmetic
-for the scale's rounding, the properties round-half-even encoding must have
+for the scale's rounding to binary16, the properties round-half-even encoding must have
 when no clamp is active, a per-key brute-force loop that reads the scale at
 each slot, constant V, and the reduction to format 2 when every row has the
 same largest value.
@@ -24,18 +24,23 @@ def _rows(rng, n, D=128, outliers=True):
     return x.astype(np.float16)
 
 
-def test_scale_is_correctly_rounded_amax_over_127():
+@pytest.mark.parametrize("amp", [1.0, 1e-3, 1e-6])     # 1e-6: scales below fp16's normal range
+def test_scale_is_correctly_rounded_amax_over_127(amp):
     rng = np.random.default_rng(1)
-    x = _rows(rng, 300)
+    x = (_rows(rng, 300).astype(np.float32) * amp).astype(np.float16)
     s = oracle.int8_row_scale(x)
     for r in range(x.shape[0]):
         amax = Fraction(max(abs(float(e)) for e in x[r]))
         exact = amax / 127
-        got = Fraction(float(s[r]))
-        # the nearest binary32 to amax/127: no other float32 is closer
-        up = Fraction(float(np.nextafter(s[r], np.float32(np.inf))))
-        dn = Fraction(float(np.nextafter(s[r], np.float32(0))))
+        h = np.float16(s[r])
+        assert float(h) == float(s[r])                   # a binary16 value
+        got = Fraction(float(h))
+        # the nearest binary16 to amax/127 (ties to even): no other fp16 is closer
+        up = Fraction(float(np.nextafter(h, np.float16(np.inf))))
+        dn = Fraction(float(np.nextafter(h, np.float16(0))))
         assert abs(got - exact) <= abs(up - exact) and abs(got - exact) <= abs(dn - exact)
+        if abs(got - exact) == abs(up - exact) or (got != 0 and abs(got - exact) == abs(dn - exact)):
+            assert (h.view(np.uint16) & 1) == 0
 
 
 def test_row_codes_equal_int8_codec_with_that_rows_scale():
@@ -67,7 +72,7 @@ def test_zero_and_nan_rows():
     x[1, 5] = -2.0
     x[2, :] = np.nan
     s = oracle.int8_row_scale(x)
-    assert s[0] == 0 and s[2] == 0 and s[1] == np.float32(2.0 / 127)
+    assert s[0] == 0 and s[2] == 0 and s[1] == np.float32(np.float16(2.0 / 127))
     c = oracle.quantize(x, s, T3).view(np.int8)
     assert (c[0] == 0).all() and (c[2] == 0).all()
     assert c[1, 3] == 0 and c[1, 5] == -127
@@ -164,7 +169,7 @@ def test_equal_row_maxima_reduce_to_one_scale_int8():
     slots = bt[0, t // P].astype(np.int64) * P + t % P
     p3, kp, vp = oracle.kv_append_quant(k, v, slots, T3, oracle.new_scale_pool(n, H, P),
                                         oracle.new_scale_pool(n, H, P), oracle.new_pool(n, H, D, T3))
-    s = np.float32(float(A) / 127)
+    s = np.float32(np.float16(float(A) / 127))          # the row scale, a binary16 value
     p2 = oracle.kv_append_quant(k, v, slots, 2, [s], [s], oracle.new_pool(n, H, D, 2))
     assert np.array_equal(p3, p2)
     q = rng.normal(0, 1, (5, 2, D)).astype(np.float16)

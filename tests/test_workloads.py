@@ -53,6 +53,10 @@ def test_workload_shapes():
     w = W.workload("e4m3_verify_512k_stress")
     assert w.seq_lens == [524288] * 2 + [32768] * 6 and w.append_tokens == 8192
     assert w.kv_bytes() == 2550136832
+    # the row-scaled INT8 pool also reads two fp16 scales per (token, kv-head)
+    w = W.workload("int8_row_decode_262k")
+    assert w.kv_bytes() == 4 * 262144 * 8 * (2 * 128 + 2 * 2)
+    assert w.append_bytes(1) == 8 * (2 * 128 * 2 + 2 * 128 + 2 * 2) + 8
 
 
 def test_plan_pool_is_a_valid_shuffled_assignment():

@@ -171,16 +171,24 @@ class Workload:
     def elem_bytes(self):
         return 2 if self.kv_dtype == FP16 else 1
 
+    @property
+    def row_scale_bytes(self):
+        """bytes of stored scale per (token, kv-head): an fp16 K and V row
+        scale for INT8_ROW, nothing for the other formats"""
+        return 4 if self.kv_dtype == INT8_ROW else 0
+
     def kv_bytes(self) -> int:
         """Algorithmic KV bytes one attention pass must read: K and V of every
-        cached token of every sequence and kv-head."""
-        return sum(self.seq_lens) * self.num_kv_heads * self.head_dim * 2 * self.elem_bytes
+        cached token of every sequence and kv-head (with their row scales)."""
+        rows = sum(self.seq_lens) * self.num_kv_heads
+        return rows * (self.head_dim * 2 * self.elem_bytes + self.row_scale_bytes)
 
     def append_bytes(self, tokens: int) -> int:
         """Algorithmic bytes of one append of ``tokens`` tokens: fp16 K and V
-        read, codes written, int64 slots read."""
+        read, codes (and row scales) written, int64 slots read."""
         n = tokens * self.num_kv_heads * self.head_dim * 2
-        return n * 2 + n * self.elem_bytes + tokens * 8
+        return (n * 2 + n * self.elem_bytes + tokens * self.num_kv_heads * self.row_scale_bytes
+                + tokens * 8)
 
 
 def workload(name: str, scale: float = 1.0) -> Workload:
