@@ -23,10 +23,12 @@ SAMPLES = {   # workload -> sampled (sequence, kv-head) segments
     "int8_decode_append_262k": [(1, 2)],
     "e4m3_decode_b8": [(3, 5), (6, 0)],
     "int8_row_decode_262k": [(2, 7)],
+    "int8_row_verify_131k": [(6, 4)],
+    "e4m3_verify_q8_131k": [(2, 3)],                 # 32 query rows per kv-head
 }
 
 
-def _oracle_segment(w, q, s, h, ks, vs):
+def _oracle_segment(w, q, s, h, ks, vs, window=0):
     """float64 output rows [q_len, G, D] of (sequence s, kv-head h)."""
     L = w.seq_lens[s]
     n = w.pages_of(L)
@@ -43,7 +45,7 @@ def _oracle_segment(w, q, s, h, ks, vs):
     G = w.group
     rows = q[s * w.q_len:(s + 1) * w.q_len, h * G:(h + 1) * G]
     return oracle.paged_attention(rows, pool, np.arange(n, dtype=np.int32)[None, :], [L],
-                                  w.q_len, w.kv_dtype, ks, vs)
+                                  w.q_len, w.kv_dtype, ks, vs, window=window)
 
 
 @pytest.mark.parametrize("name", list(SAMPLES))
@@ -66,5 +68,27 @@ def test_full_size_sampled_segments(name):
         ref = _oracle_segment(w, q, s, h, ks, vs)
         got = out[s * w.q_len:(s + 1) * w.q_len, h * G:(h + 1) * G]
         assert_close(got, ref, "%s seq %d head %d" % (name, s, h))
+    del c
+    torch.cuda.empty_cache()
+
+
+def test_full_size_sliding_window_sampled_segments():
+    # the 131K verify with the 2048-token window bench.py times beside it
+    pq = require_gpu()
+    w = W.workload("e4m3_verify_131k")
+    c = Case(w, with_oracle=False)
+    out = torch.full_like(c.q, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pq.paged_attention(c.q, c.pages, c.bt, c.seq_lens, w.q_len, w.kv_dtype, c.ks, c.vs, out,
+                       num_splits=0, window=2048, status=status, max_seq_len=max(w.seq_lens))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    out = out.float().cpu().numpy()
+    q = c.q.cpu().numpy()
+    G = w.group
+    for s, h in [(1, 5), (7, 0)]:
+        ref = _oracle_segment(w, q, s, h, float(c.ks.cpu()[0]), float(c.vs.cpu()[0]), window=2048)
+        got = out[s * w.q_len:(s + 1) * w.q_len, h * G:(h + 1) * G]
+        assert_close(got, ref, "window 2048 seq %d head %d" % (s, h))
     del c
     torch.cuda.empty_cache()
