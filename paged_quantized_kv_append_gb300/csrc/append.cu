@@ -37,9 +37,10 @@
 //
 // INT8 with a scale per row (the README's INT8 KV with run-time scales): the
 // eight threads of a row -- eight consecutive lanes of one warp -- exchange
-// their partial |x| maxima with shuffles, divide the row maximum by 127, encode
-// under that scale and the row's first thread stores the scale at the row's
-// slot of the scale area that follows the codes.
+// their partial |x| maxima with shuffles, round the row maximum over 127 to
+// the nearest fp16 value, encode under that scale and the row's first thread
+// stores the fp16 scale at the row's place in the scale area that follows the
+// codes.
 #include <atomic>
 
 #include "pqkv_common.cuh"
