@@ -168,7 +168,13 @@ def row_scales(pages: torch.Tensor) -> torch.Tensor:
     whole = torch.empty(0, dtype=torch.uint8, device=pages.device)
     whole.set_(pages.untyped_storage(), pages.storage_offset(),
                (codes + _row_scale_bytes(n, H),))
-    return whole[codes:].view(torch.float16).view(n, H, 8, 2, 2).permute(0, 1, 3, 4, 2)
+    return _row_scale_view(whole[codes:], n, H)
+
+
+def _row_scale_view(area: torch.Tensor, num_pages: int, num_kv_heads: int) -> torch.Tensor:
+    """[p, h, kv, r // 8, r % 8] view of a scale area (uint8 bytes) stored as
+    fp16 [p][h][i][4] = (K row i, K row i+8, V row i, V row i+8)."""
+    return area.view(torch.float16).view(num_pages, num_kv_heads, 8, 2, 2).permute(0, 1, 3, 4, 2)
 
 
 def _check_pages(pages, kd):

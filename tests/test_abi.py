@@ -190,3 +190,26 @@ def test_binding_signatures_match_the_header(lib):
         fn = getattr(lib, name)
         assert fn.argtypes is not None, name
         assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
+def test_row_scale_view_follows_the_header_layout():
+    # fp16 row_scale[p][h][i][4]: K row i, K row i+8, V row i, V row i+8
+    import numpy as np
+    import torch
+    n, H = 3, 2
+    flat = np.zeros(n * H * 32, np.float16)
+    for p in range(n):
+        for h in range(H):
+            for r in range(16):
+                for kv in range(2):
+                    j = 2 * kv + r // 8
+                    flat[((p * H + h) * 8 + r % 8) * 4 + j] = p * 100 + h * 40 + kv * 20 + r
+    area = torch.from_numpy(flat.view(np.uint8).copy())
+    view = pq._row_scale_view(area, n, H)
+    assert tuple(view.shape) == (n, H, 2, 2, 8)
+    rows = view.reshape(n, H, 2, 16).numpy()
+    want = (np.arange(n)[:, None, None, None] * 100 + np.arange(H)[None, :, None, None] * 40
+            + np.arange(2)[None, None, :, None] * 20 + np.arange(16)[None, None, None, :])
+    assert np.array_equal(rows.astype(np.int64), want)
+    view[1, 0, 1, 1, 3] = -7                    # V row 11 of page 1, head 0 writes through
+    assert area.view(torch.float16)[((1 * H + 0) * 8 + 3) * 4 + 3].item() == -7
